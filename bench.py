@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Benchmark of the GEMM hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over the headline workload,
+M = N = 8192, K = 4096, row-major, synthetic seeded operands:
+  * gemm_f32    FP32 SIMT      A, B uniform[-1, 1) f32, C = 0, alpha = 1, beta = 0
+  * gemm_tf32   TF32 tcgen05   same operands
+  * gemm_f16_tn FP16 TN tcgen05, A, B ~ N(0,1)/sqrt(K) in f16, FP32 accumulate
+value = 3 * 2MNK / (sum of the three kernels' device times), in TFLOP/s,
+summed over ranks; the per-path TFLOP/s and fractions of peak are in "paths".
+
+Timing: CUDA events on the launching stream around each GEMM; before every
+GEMM a 512 MiB buffer is written to flush the 129 MB L2 (outside the events).
+The e2e number runs the same GEMMs through the public API with the operands
+in pinned host memory: host->device copies of A and B, the call, and the
+device->host copy of C are all inside its timed region.
+
+--impl reference times the CPU oracle (the only other implementation of the
+method here) on a bounded sample of the same workload: full rows of C for
+each path, as many as fit in a fixed time budget per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M = N = 8192
+K = 4096
+FLOPS = 2.0 * M * N * K
+PATHS = ("f32_simt", "tf32", "f16_tn")
+
+# Peaks (TFLOP/s).  FP32 SIMT: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz.
+SM_COUNT_NOMINAL = 152
+SM_MAX_MHZ_NOMINAL = 2070.0
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def _peaks():
+    peaks_file = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    src = "fallback"
+    bf16, bf16_sus, hbm = 1900.0, 1700.0, 6800.0
+    if os.path.exists(peaks_file):
+        with open(peaks_file) as f:
+            d = json.load(f)
+        bf16 = float(d.get("bf16_tflops", bf16))
+        bf16_sus = float(d.get("bf16_tflops_sustained", bf16_sus))
+        hbm = float(d.get("hbm_gbs", hbm))
+        src = "measured"
+    return {"f16_tn": bf16, "tf32": bf16 * NOMINAL_TF32_OVER_BF16,
+            "f32_simt": SM_COUNT_NOMINAL * 128 * 2 * SM_MAX_MHZ_NOMINAL * 1e6 / 1e12,
+            "source": src, "hbm_gbs": hbm, "bf16_sustained": bf16_sus}
+
+
+# Targets' denominators as recorded with the workload definition (datasheet-class).
+DATASHEET = {"f16_tn": 2250.0, "tf32": 1100.0, "f32_simt": 77.5}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _traffic_for(kernel_file: str, kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, only if the
+    kernel source has not changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "dense_gemm_09_gb300", "csrc", kernel_file)
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    return e.get("bytes_per_launch") if e.get("source_sha256") == sha else None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import dense_gemm_09_gb300 as dg
+    import seeded_inputs as si
+
+    world, rank, local = _dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    dg.lib()
+    stream = torch.cuda.current_stream()
+
+    # operands: one seeded problem per rank (replicas, weak scaling)
+    w32 = si.WORKLOADS["f32_8192x8192x4096"]
+    w16 = si.WORKLOADS["f16_tn_8192x8192x4096"]
+    A32h, B32h, _ = si.make(w32, seed=rank, pin=True)
+    A16h, B16h, _ = si.make(w16, seed=rank, pin=True)
+    A32, B32 = A32h.to(dev), B32h.to(dev)
+    A16, B16 = A16h.to(dev), B16h.to(dev)
+    C32 = torch.zeros((M, N), dtype=torch.float32, device=dev)
+    C16 = torch.zeros((M, N), dtype=torch.float16, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    calls = {
+        "f32_simt": lambda: dg.gemm_f32(A32, B32, C32, 1.0, 0.0, stream=stream),
+        "tf32": lambda: dg.gemm_tf32(A32, B32, C32, 1.0, 0.0, stream=stream),
+        "f16_tn": lambda: dg.gemm_f16_tn(A16, B16, C16, 1.0, 0.0, stream=stream),
+    }
+    kernels = {}
+
+    def step(record):
+        for p in PATHS:
+            flush.zero_()
+            if record is not None:
+                record[p][0].record(stream)
+            calls[p]()
+            if record is not None:
+                record[p][1].record(stream)
+            kernels[p] = dg.last_kernel()
+
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize()
+
+    events = [{p: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for p in PATHS} for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            step(events[s])
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    per_path = {p: [events[s][p][0].elapsed_time(events[s][p][1]) for s in range(args.steps)]
+                for p in PATHS}
+    ms_step_local = sum(statistics.mean(v) for v in per_path.values())
+    ms_step = _max_over_ranks(ms_step_local, world, dev)
+    total_flops = 3 * FLOPS * world
+    value = total_flops / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API, operands in pinned host memory
+    C32h = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    C16h = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    h2d = 2 * (A32h.numel() * 4 + B32h.numel() * 4) + A16h.numel() * 2 + B16h.numel() * 2
+    d2h = 2 * C32h.numel() * 4 + C16h.numel() * 2
+
+    def e2e_step():
+        for p, (Ah, Bh, Ad, Bd, Cd, Ch) in (
+                ("f32_simt", (A32h, B32h, A32, B32, C32, C32h)),
+                ("tf32", (A32h, B32h, A32, B32, C32, C32h)),
+                ("f16_tn", (A16h, B16h, A16, B16, C16, C16h))):
+            Ad.copy_(Ah, non_blocking=True)
+            Bd.copy_(Bh, non_blocking=True)
+            calls[p]()
+            Ch.copy_(Cd, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
+    assert dg.device_status() == dg.OK
+
+    peaks = _peaks()
+    paths = {}
+    for p in PATHS:
+        ms = statistics.mean(per_path[p])
+        tf = FLOPS / (ms * 1e-3) / 1e12
+        paths[p] = {"kernel": kernels[p], "ms": round(ms, 4), "ms_min": round(min(per_path[p]), 4),
+                    "tflops": round(tf, 2), "peak_tflops": round(peaks[p], 1),
+                    "frac_of_peak": round(tf / peaks[p], 4),
+                    "frac_of_datasheet": round(tf / DATASHEET[p], 4)}
+    dominant = max(PATHS, key=lambda p: paths[p]["ms"])
+    dom = paths[dominant]
+    kfile = "sgemm_simt.cu" if dominant == "f32_simt" else "umma_gemm.cu"
+    roofline = {"kernel": dom["kernel"],
+                "bound": "alu" if dominant == "f32_simt" else "tensor",
+                "achieved": dom["tflops"], "peak": dom["peak_tflops"], "unit": "TFLOP/s",
+                "frac": dom["frac_of_peak"],
+                "peak_source": ("derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz"
+                                if dominant == "f32_simt" else peaks["source"] + " (MEASURED_PEAKS.json)"),
+                "traffic": _traffic_for(kfile, dom["kernel"])}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(budget_s=args.cpu_budget)
+
+    clocks = clk.summary()
+    line = {
+        "metric": "GEMM TFLOPS (2MNK/s) per dtype at M=N=8192,K=4096; % of dense peak",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32+tf32+f16(f32 acc)",
+        "data": "synthetic (seeded uniform[-1,1) f32; N(0,1)/sqrt(K) f16)",
+        "config": {"workload": "gemm_f32_tf32_f16tn_8192x8192x4096", "M": M, "N": N, "K": K,
+                   "alpha": 1.0, "beta": 0.0, "layout": "row-major NN (f32, tf32); TN (f16)",
+                   "step": "gemm_f32 + gemm_tf32 + gemm_f16_tn, one each",
+                   "l2": "flushed before every GEMM (512 MiB write, outside the timed events)",
+                   "parallelism": "replicas x%d" % world},
+        "paths": paths,
+        "roofline": roofline,
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "how": "pinned host A,B -> device copies, the C-ABI call, C -> pinned host; per path"},
+        "gpu_launches": 3 * args.steps,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+_ORACLE_OPERANDS = {}
+
+
+def _oracle_operands():
+    """Widened (double) operands of the headline workload, built once; the
+    widening is set-up and is not part of any timed sample."""
+    if not _ORACLE_OPERANDS:
+        import oracle
+        import seeded_inputs as si
+        A32, B32, _ = si.make(si.WORKLOADS["f32_8192x8192x4096"], seed=0)
+        A16, B16, _ = si.make(si.WORKLOADS["f16_tn_8192x8192x4096"], seed=0)
+        A32, B32 = A32.numpy(), B32.numpy()
+        _ORACLE_OPERANDS.update({
+            "f32_simt": (oracle.widen("f32", A32), oracle.widen("f32", B32)),
+            "tf32": (oracle.widen("tf32_rna", A32), oracle.widen("tf32_rna", B32)),
+            "f16_tn": (oracle.widen("f16", A16.numpy()), oracle.widen("f16", B16.numpy(), trans=True)),
+        })
+    return _ORACLE_OPERANDS
+
+
+def _oracle_rows_sample(budget_s: float, nthreads: int = 0):
+    """Oracle TFLOP rate on full rows of C for each path, within budget_s."""
+    import numpy as np
+
+    import oracle
+
+    operands = _oracle_operands()
+    threads = nthreads or os.cpu_count() or 1
+    per = budget_s / 3.0
+    rows_done, secs = 0, 0.0
+    chunk = max(threads, 16)
+    for p in PATHS:
+        A64, B64 = operands[p]
+        start = time.perf_counter()
+        r = 0
+        while time.perf_counter() - start < per:
+            rows = np.arange(r, r + chunk, dtype=np.int64) % M
+            oracle.gemm(A64, B64, None, 1.0, 0.0, rows=rows, nthreads=threads)
+            r += chunk
+        secs += time.perf_counter() - start
+        rows_done += r
+    flops = 2.0 * rows_done * N * K
+    return flops / secs / 1e12, threads, rows_done, secs
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    tflops, threads, rows, secs = _oracle_rows_sample(budget_s)
+    return {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "%d full rows of C (x N=8192, K=4096) across the three paths in %.1f s; "
+                      "operand widening to double not timed" % (rows, secs)}
+
+
+def run_reference(args):
+    world, rank, _ = _dist_setup()
+    if rank != 0:
+        return
+    # each step: a bounded sample of the workload on the oracle, sized so the
+    # whole run stays within a few minutes
+    budget = min(args.cpu_budget, 150.0 / max(args.steps, 1))
+    for _ in range(args.warmup):
+        _oracle_rows_sample(min(budget, 3.0))
+    rates, total_rows, total_s, threads = [], 0, 0.0, 1
+    for _ in range(args.steps):
+        tf, threads, rows, secs = _oracle_rows_sample(budget)
+        rates.append(tf)
+        total_rows += rows
+        total_s += secs
+    value = statistics.mean(rates)
+    line = {
+        "impl": "reference",
+        "metric": "GEMM TFLOPS (2MNK/s) per dtype at M=N=8192,K=4096; % of dense peak",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / max(args.steps, 1), 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 accumulation over f32 / tf32 / f16 operand values",
+        "data": "synthetic (seeded uniform[-1,1) f32; N(0,1)/sqrt(K) f16)",
+        "config": {"workload": "gemm_f32_tf32_f16tn_8192x8192x4096", "M": M, "N": N, "K": K,
+                   "alpha": 1.0, "beta": 0.0},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "%d full rows of C over %d steps (%.1f s per step budget)"
+                                   % (total_rows, args.steps, budget)},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work per CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

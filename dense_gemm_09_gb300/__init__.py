@@ -1,0 +1,145 @@
+"""Python binding of libdgemm (include/dgemm.h): dense row-major GEMM on GB300.
+
+Argument marshalling only: every entry point takes torch CUDA tensors, reads
+their data pointers, row pitches and the current stream, and calls the C ABI
+of the same name.  All arithmetic runs in the library's CUDA kernels; there
+is no fallback of any kind -- if the library is missing or the call fails,
+an exception is raised.
+
+    gemm_f32(A, B, C, alpha, beta)     C = alpha*A@B + beta*C     (FP32, CUDA cores)
+    gemm_tf32(A, B, C, alpha, beta)    same, TF32 tensor cores   (FP32 in / out)
+    gemm_f16_tn(A, B, C, alpha, beta)  C = alpha*A@B.T + beta*C  (FP16 in / out,
+                                                                   FP32 accumulate)
+
+Matrices are 2-D tensors with unit column stride; a row stride larger than
+the width is passed on as the leading dimension.  C is updated in place and
+returned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdgemm.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DgemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+def build(force: bool = False) -> str:
+    """Compile libdgemm.so (nvcc, sm_103a) in-tree."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded C library, with its signatures declared."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libdgemm.so is not built (%s); run dense_gemm_09_gb300.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        i64, f32, vp, ci = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
+        sig = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        for name in ("gemm_f32", "gemm_tf32", "gemm_f16_tn"):
+            fn = getattr(L, name)
+            fn.argtypes = sig
+            fn.restype = ci
+        L.dgemm_status_string.argtypes = [ci]
+        L.dgemm_status_string.restype = ctypes.c_char_p
+        L.dgemm_device_status.argtypes = [ci]
+        L.dgemm_device_status.restype = ci
+        L.dgemm_last_kernel.argtypes = []
+        L.dgemm_last_kernel.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().dgemm_status_string(int(status)).decode()
+
+
+def device_status(clear: bool = True) -> int:
+    """The kernels' device status word (synchronises the device)."""
+    return lib().dgemm_device_status(1 if clear else 0)
+
+
+def last_kernel() -> str:
+    """Name of the kernel variant the last call on this thread launched."""
+    return lib().dgemm_last_kernel().decode()
+
+
+def _mat(t: torch.Tensor, name: str, dtype: torch.dtype):
+    if not isinstance(t, torch.Tensor) or t.dim() != 2:
+        raise ValueError("%s must be a 2-D tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    rows, cols = t.shape
+    if cols > 1 and t.stride(1) != 1:
+        raise ValueError("%s must have unit column stride" % name)
+    ld = t.stride(0) if rows > 1 else cols
+    return t.data_ptr(), max(ld, cols)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _call(name, M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, stream):
+    st = getattr(lib(), name)(M, N, K, float(alpha), pa, lda, pb, ldb, float(beta), pc, ldc,
+                              _stream(stream))
+    if st != OK:
+        raise DgemmError(st, name)
+
+
+def _nn(name, A, B, C, alpha, beta, stream):
+    pa, lda = _mat(A, "A", torch.float32)
+    pb, ldb = _mat(B, "B", torch.float32)
+    pc, ldc = _mat(C, "C", torch.float32)
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch: A %s, B %s, C %s" % (tuple(A.shape), tuple(B.shape), tuple(C.shape)))
+    _call(name, M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, stream)
+    return C
+
+
+def gemm_f32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B + beta * C on the FP32 pipes (A: M x K, B: K x N)."""
+    return _nn("gemm_f32", A, B, C, alpha, beta, stream)
+
+
+def gemm_tf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B + beta * C with TF32 tensor-core products."""
+    return _nn("gemm_tf32", A, B, C, alpha, beta, stream)
+
+
+def gemm_f16_tn(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B.T + beta * C; A: M x K, B: N x K, C: M x N, all f16."""
+    pa, lda = _mat(A, "A", torch.float16)
+    pb, ldb = _mat(B, "B", torch.float16)
+    pc, ldc = _mat(C, "C", torch.float16)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch: A %s, B %s, C %s" % (tuple(A.shape), tuple(B.shape), tuple(C.shape)))
+    _call("gemm_f16_tn", M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, stream)
+    return C

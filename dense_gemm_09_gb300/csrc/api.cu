@@ -1,0 +1,141 @@
+// api.cu -- the C ABI declared in include/dgemm.h: argument validation on
+// the host, the device check, the special cases (M or N empty; K == 0 or
+// alpha == 0) and dispatch to the kernels.  Nothing here allocates device
+// memory or synchronises (except dgemm_device_status, which says so).
+//
+// The pages' host launchers ("SGEMM CUDA代码学习", its torch bindings) check
+// dtype and shape and throw; here every check returns a status before any
+// launch, and launch errors are reported instead of ignored.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "dgemm.h"
+#include "internal.h"
+
+namespace dgemm {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+thread_local const char *t_last_kernel = "";
+
+// Per-device properties, filled on first use.
+bool device_info(DeviceInfo &out)
+{
+    static DeviceInfo cache[kMaxDevices];
+    static std::once_flag once[kMaxDevices];
+    static bool valid[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::call_once(once[dev], [dev] {
+        DeviceInfo d;
+        bool ok = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
+                      cudaSuccess;
+        cache[dev] = d;
+        valid[dev] = ok;
+    });
+    out = cache[dev];
+    return valid[dev];
+}
+
+int check_device(DeviceInfo &dev)
+{
+    if (!device_info(dev)) return DGEMM_ERR_UNSUPPORTED_DEVICE;
+    if (dev.major != 10 || dev.minor != 3) return DGEMM_ERR_UNSUPPORTED_DEVICE;
+    return DGEMM_OK;
+}
+
+// Validation common to all entry points.  b_row_len is the length of a
+// stored row of B (N for NN, K for TN).
+int validate(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+             const void *B, int64_t ldb, int64_t b_row_len, const void *C, int64_t ldc)
+{
+    if (M < 0 || N < 0 || K < 0) return DGEMM_ERR_INVALID_ARG;
+    if (lda < K || ldb < b_row_len || ldc < N) return DGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DGEMM_OK;
+    if (!C) return DGEMM_ERR_INVALID_ARG;
+    const bool reads_ab = K > 0 && alpha != 0.f;
+    if (reads_ab && (!A || !B)) return DGEMM_ERR_INVALID_ARG;
+    return DGEMM_OK;
+}
+
+int finish(const char *name)
+{
+    if (!name) return DGEMM_ERR_LAUNCH;
+    const cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return DGEMM_ERR_LAUNCH;
+    t_last_kernel = name;
+    return DGEMM_OK;
+}
+
+}  // namespace
+}  // namespace dgemm
+
+using namespace dgemm;
+
+extern "C" int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                        const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                        cudaStream_t stream)
+{
+    int st = validate(M, N, K, alpha, A, lda, B, ldb, N, C, ldc);
+    if (st != DGEMM_OK || M == 0 || N == 0) return st;
+    DeviceInfo dev;
+    if ((st = check_device(dev)) != DGEMM_OK) return st;
+    if (K == 0 || alpha == 0.f) return finish(launch_scale_f32(M, N, beta, C, ldc, stream));
+    return finish(launch_sgemm_simt(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream));
+}
+
+extern "C" int gemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                         const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                         cudaStream_t stream)
+{
+    int st = validate(M, N, K, alpha, A, lda, B, ldb, N, C, ldc);
+    if (st != DGEMM_OK || M == 0 || N == 0) return st;
+    DeviceInfo dev;
+    if ((st = check_device(dev)) != DGEMM_OK) return st;
+    if (K == 0 || alpha == 0.f) return finish(launch_scale_f32(M, N, beta, C, ldc, stream));
+    return finish(launch_umma_tf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev));
+}
+
+extern "C" int gemm_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
+                           int64_t lda, const uint16_t *B, int64_t ldb, float beta, uint16_t *C,
+                           int64_t ldc, cudaStream_t stream)
+{
+    int st = validate(M, N, K, alpha, A, lda, B, ldb, K, C, ldc);
+    if (st != DGEMM_OK || M == 0 || N == 0) return st;
+    DeviceInfo dev;
+    if ((st = check_device(dev)) != DGEMM_OK) return st;
+    if (K == 0 || alpha == 0.f) return finish(launch_scale_f16(M, N, beta, C, ldc, stream));
+    return finish(launch_umma_f16_tn(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev));
+}
+
+extern "C" const char *dgemm_status_string(int status)
+{
+    switch (status) {
+    case DGEMM_OK: return "DGEMM_OK: success";
+    case DGEMM_ERR_INVALID_ARG: return "DGEMM_ERR_INVALID_ARG: invalid size, leading dimension or pointer";
+    case DGEMM_ERR_UNSUPPORTED_DEVICE: return "DGEMM_ERR_UNSUPPORTED_DEVICE: current device is not sm_103 (GB300)";
+    case DGEMM_ERR_LAUNCH: return "DGEMM_ERR_LAUNCH: the CUDA runtime reported a launch error";
+    case DGEMM_ERR_TIMEOUT: return "DGEMM_ERR_TIMEOUT: a kernel wait ran out and the kernel exited early";
+    default: return "unknown dgemm status";
+    }
+}
+
+extern "C" int dgemm_device_status(int clear)
+{
+    DeviceInfo dev;
+    int st = check_device(dev);
+    if (st != DGEMM_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DGEMM_ERR_LAUNCH;
+    return umma_read_status(clear);
+}
+
+extern "C" const char *dgemm_last_kernel(void)
+{
+    return t_last_kernel;
+}

@@ -1,0 +1,48 @@
+// internal.h -- declarations shared between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace dgemm {
+
+inline bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// Each launcher enqueues its kernel(s) on `stream` and returns the name of
+// the variant it chose.  Arguments have been validated by the caller.
+
+const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                              int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                              int64_t ldc, cudaStream_t stream);
+
+// C = beta * C (beta == 0: C = 0), for K == 0 or alpha == 0.
+const char *launch_scale_f32(int64_t M, int64_t N, float beta, float *C, int64_t ldc,
+                             cudaStream_t stream);
+const char *launch_scale_f16(int64_t M, int64_t N, float beta, uint16_t *C, int64_t ldc,
+                             cudaStream_t stream);
+
+struct DeviceInfo {
+    int major = 0, minor = 0;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+};
+
+// Tensor-core paths.  Return nullptr if the launch could not be prepared
+// (e.g. the driver's tensor-map encoder is unavailable).
+const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
+                               int64_t lda, const uint16_t *B, int64_t ldb, float beta,
+                               uint16_t *C, int64_t ldc, cudaStream_t stream,
+                               const DeviceInfo &dev);
+const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                             int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                             int64_t ldc, cudaStream_t stream, const DeviceInfo &dev);
+
+// Device status word of the tensor-core kernels (see dgemm_device_status).
+int umma_read_status(int clear);
+
+}  // namespace dgemm

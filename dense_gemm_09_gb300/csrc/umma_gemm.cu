@@ -1,0 +1,539 @@
+// umma_gemm.cu -- tensor-core GEMM for sm_103a on tcgen05 (5th-generation
+// tensor cores, accumulators in tensor memory), for two input types:
+//
+//   FP16 TN : C(f16) = alpha * A * B^T + beta * C, A M x K and B N x K
+//             row-major (both K-major), FP32 accumulation;
+//   TF32    : C(f32) = alpha * A * B + beta * C, A M x K (K-major) and
+//             B K x N row-major (N-major), operands read as TF32.
+//
+// Structure -- a persistent, warp-specialised kernel, one CTA per SM:
+//   warp 0      TMA producer: one thread streams 128 x BK tiles of A and
+//               BK x 256 tiles of B into a 4-stage shared-memory ring
+//               (128-byte swizzled rows), signalling "full" mbarriers with
+//               transaction byte counts;
+//   warp 1      MMA issuer: one thread waits for a full stage, issues
+//               BK/UMMA_K tcgen05.mma instructions of 128 x 256 x UMMA_K into
+//               a TMEM accumulator, and commits the stage back to its
+//               "empty" mbarrier when those MMAs have read it;
+//   warps 2..5  epilogue: drain the accumulator TMEM -> registers
+//               (tcgen05.ld), form alpha * acc + beta * C_old in FP32 and
+//               store with 16-byte vectors, masked at the M / N edges.
+// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile run
+// while the MMAs of the next tile proceed.
+//
+// This is the GB300 form of the pages' designs:
+//   * the producer / consumer split with a stage ring and acquire / release
+//     primitives -- "Warp Specialization HGEMM", sections "1. 角色划分" to
+//     "4. consumer 的双重流水" (cuda::pipeline there, mbarriers here);
+//   * the XOR smem swizzle of "HGEMM SMEM Swizzle 代码学习" ("swizzle 核心"),
+//     here the hardware 128-byte swizzle written by TMA and read by the MMA
+//     through the matching descriptor mode;
+//   * the multi-stage async-copy ring of "SGEMM CUDA代码学习", "第 5 步"
+//     (cp.async + wait_group there, TMA + mbarrier transaction counts here);
+//   * block-order swizzling for L2 reuse ("第 5 步", block swizzle), here the
+//     persistent scheduler's grouped tile order.
+// Tails: TMA fills out-of-range rows / columns / K with zeros, which add
+// exact zeros to the sums, and the epilogue masks stores outside M x N.
+//
+// Every mbarrier wait is bounded (a few seconds of %globaltimer): a wait that
+// runs out records DGEMM_ERR_TIMEOUT in the device status word, raises an
+// abort flag that the other roles also poll, waits (again bounded) for its
+// own copies and MMAs in flight, and the CTA releases its TMEM and exits.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "dgemm.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dgemm {
+
+__device__ int g_umma_status;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int ROW_BYTES = 128;                     // one swizzled row
+constexpr int A_TILE_BYTES = BM * ROW_BYTES;       // 16 KB
+constexpr int B_TILE_BYTES = BN * ROW_BYTES;       // 32 KB
+constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int TMEM_COLS = 2 * BN;                  // two f32 accumulators
+constexpr int kGroupN = 8;                         // tile-order group width
+constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s
+constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
+
+enum { kF16 = 0, kTF32 = 1 };
+
+template <int kKind>
+struct Traits;
+template <>
+struct Traits<kF16> {
+    static constexpr int kElem = 2;
+    static constexpr int BK = ROW_BYTES / kElem;  // 64
+    static constexpr int UMMA_K = 16;             // 32 bytes of K per MMA
+    // D = f32 (bits 4-5 = 1), A = B = f16 (0), both K-major, N >> 3, M >> 4.
+    static constexpr uint32_t kIdesc =
+        (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+};
+template <>
+struct Traits<kTF32> {
+    static constexpr int kElem = 4;
+    static constexpr int BK = ROW_BYTES / kElem;  // 32
+    static constexpr int UMMA_K = 8;              // 32 bytes of K per MMA
+    // D = f32, A = B = tf32 (code 2), A K-major, B N-major (bit 16).
+    static constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (1u << 16) |
+                                       (static_cast<uint32_t>(BN >> 3) << 17) |
+                                       (static_cast<uint32_t>(BM >> 4) << 24);
+};
+
+struct Ctrl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + static_cast<int>(sizeof(Ctrl));
+
+struct Params {
+    int64_t M, N, K;
+    float alpha, beta;
+    void *C;
+    int64_t ldc;
+    int64_t tiles_m, tiles_n, num_kb;
+    int vec_c;
+};
+
+__device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t &m0, int64_t &n0)
+{
+    // Groups of kGroupN tile columns; inside a group consecutive tiles share
+    // one A row band and walk N, so the tiles in flight at once read a few
+    // B column bands and a few A row bands.
+    const int64_t per_group = static_cast<int64_t>(kGroupN) * p.tiles_m;
+    const int64_t g = t / per_group, r = t % per_group;
+    const int64_t left = p.tiles_n - g * kGroupN;
+    const int64_t gn = left < kGroupN ? left : kGroupN;
+    n0 = (g * kGroupN + r % gn) * BN;
+    m0 = (r / gn) * BM;
+}
+
+__device__ __forceinline__ void raise_abort(volatile int *abort_flag)
+{
+    if (atomicExch(&g_umma_status, DGEMM_ERR_TIMEOUT) == 0) __threadfence();
+    *abort_flag = 1;
+}
+
+// Bounded wait for the phase of the given parity; false on time-out or when
+// another role raised the abort flag.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            raise_abort(abort_flag);
+            return false;
+        }
+    }
+}
+
+// Bounded wait used on the way out, after an abort: ignores the abort flag.
+__device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) return false;
+    return true;
+}
+
+template <int kKind>
+__device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
+                                             const Params &p, uint32_t smem_base, Ctrl *ctrl,
+                                             volatile int *abort_flag)
+{
+    using T = Traits<kKind>;
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued = 0, issued_phase = 0;  // per-stage: a load was issued / its phase
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int64_t m0, n0;
+        tile_coords(t, p, m0, n0);
+        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint32_t full = ptx::smem_addr(&ctrl->full[stage]);
+            ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+            const uint32_t sa = smem_base + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_TILE_BYTES;
+            const int32_t kc = static_cast<int32_t>(kb * T::BK);
+            ptx::tma_load_2d(sa, tmap_a, full, kc, static_cast<int32_t>(m0));
+            if constexpr (kKind == kF16) {
+                ptx::tma_load_2d(sb, tmap_b, full, kc, static_cast<int32_t>(n0));
+            } else {
+                // B is N-major: eight 32(N) x 32(K) boxes, one 4 KB swizzle
+                // column each.
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+                    ptx::tma_load_2d(sb + c * 4096, tmap_b, full,
+                                     static_cast<int32_t>(n0 + c * 32), kc);
+            }
+            issued |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        // Do not leave while TMA may still be writing into this CTA's smem.
+        for (int s = 0; s < STAGES; ++s)
+            if ((issued >> s) & 1u)
+                drain_wait(ptx::smem_addr(&ctrl->full[s]), (issued_phase >> s) & 1u);
+    }
+}
+
+template <int kKind>
+__device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctrl *ctrl,
+                                        uint32_t tmem_base, volatile int *abort_flag)
+{
+    using T = Traits<kKind>;
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        if (!wait_bounded(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bounded(ptx::smem_addr(&ctrl->full[stage]), phase, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sa = smem_base + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_TILE_BYTES;
+#pragma unroll
+            for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
+                // A (K-major): advance 32 bytes along the swizzled row.
+                const uint64_t da = ptx::sw128_desc(sa + k * 32, 16, 1024);
+                uint64_t db;
+                if constexpr (kKind == kF16)
+                    db = ptx::sw128_desc(sb + k * 32, 16, 1024);
+                else  // B (N-major): next 8 K-rows; 4 KB between 32-wide N columns
+                    db = ptx::sw128_desc(sb + k * 1024, 4096, 1024);
+                ptx::umma<kKind>(d_tmem, da, db, T::kIdesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            ptx::umma_commit(ptx::smem_addr(&ctrl->empty[stage]));
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        ptx::umma_commit(ptx::smem_addr(&ctrl->tmem_full[acc]));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    // Every MMA this thread issued has finished before TMEM can be released.
+    ptx::umma_commit(ptx::smem_addr(&ctrl->mma_done));
+    drain_wait(ptx::smem_addr(&ctrl->mma_done), 0);
+}
+
+__device__ __forceinline__ float as_f(uint32_t u)
+{
+    return __uint_as_float(u);
+}
+
+// Store 32 consecutive accumulator columns of one row.
+template <int kKind>
+__device__ __forceinline__ void store_chunk(const Params &p, int64_t row, int64_t col,
+                                            const uint32_t (&r)[32])
+{
+    if (row >= p.M) return;
+    const float alpha = p.alpha, beta = p.beta;
+    if constexpr (kKind == kF16) {
+        __half *crow = reinterpret_cast<__half *>(p.C) + row * p.ldc;
+        if (p.vec_c && col + 31 < p.N) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 *dst = reinterpret_cast<uint4 *>(crow + col + q * 8);
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = alpha * as_f(r[q * 8 + e]);
+                if (beta != 0.f) {
+                    const uint4 old = *dst;
+                    const __half2 *h = reinterpret_cast<const __half2 *>(&old);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(h[e]);
+                        v[2 * e] = fmaf(beta, f.x, v[2 * e]);
+                        v[2 * e + 1] = fmaf(beta, f.y, v[2 * e + 1]);
+                    }
+                }
+                uint4 out;
+                __half2 *o = reinterpret_cast<__half2 *>(&out);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+                *dst = out;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                if (col + e < p.N) {
+                    float v = alpha * as_f(r[e]);
+                    if (beta != 0.f) v = fmaf(beta, __half2float(crow[col + e]), v);
+                    crow[col + e] = __float2half_rn(v);
+                }
+            }
+        }
+    } else {
+        float *crow = reinterpret_cast<float *>(p.C) + row * p.ldc;
+        if (p.vec_c && col + 31 < p.N) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 *dst = reinterpret_cast<float4 *>(crow + col + q * 4);
+                float4 v = make_float4(alpha * as_f(r[q * 4 + 0]), alpha * as_f(r[q * 4 + 1]),
+                                       alpha * as_f(r[q * 4 + 2]), alpha * as_f(r[q * 4 + 3]));
+                if (beta != 0.f) {
+                    const float4 c = *dst;
+                    v.x = fmaf(beta, c.x, v.x);
+                    v.y = fmaf(beta, c.y, v.y);
+                    v.z = fmaf(beta, c.z, v.z);
+                    v.w = fmaf(beta, c.w, v.w);
+                }
+                *dst = v;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                if (col + e < p.N) {
+                    float v = alpha * as_f(r[e]);
+                    if (beta != 0.f) v = fmaf(beta, crow[col + e], v);
+                    crow[col + e] = v;
+                }
+            }
+        }
+    }
+}
+
+template <int kKind>
+__device__ __forceinline__ void run_epilogue(const Params &p, Ctrl *ctrl, uint32_t tmem_base,
+                                             int warp, int lane, volatile int *abort_flag)
+{
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const uint32_t quarter = static_cast<uint32_t>(warp & 3);  // TMEM lanes this warp may read
+    uint32_t acc = 0, acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int64_t m0, n0;
+        tile_coords(t, p, m0, n0);
+        bool ok = wait_bounded(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const int64_t row = m0 + quarter * 32 + lane;
+        const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            __syncwarp();  // tcgen05.ld is warp-collective (.sync.aligned)
+            ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+            ptx::tmem_ld_wait();
+            store_chunk<kKind>(p, row, n0 + c * 32, r);
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_addr(&ctrl->tmem_empty[acc]));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+}
+
+template <int kKind>
+__global__ void __launch_bounds__(THREADS, 1)
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                     const __grid_constant__ CUtensorMap tmap_b, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + STAGES * STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&ctrl->full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_full[a]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_empty[a]), 4 * 32);
+        }
+        ptx::mbar_init(ptx::smem_addr(&ctrl->mma_done), 1);
+        ctrl->abort = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmap_a);
+        ptx::prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(&ctrl->tmem_base), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = ctrl->tmem_base;
+    volatile int *abort_flag = &ctrl->abort;
+    const uint32_t smem_base = ptx::smem_addr(smem);
+
+    if (warp == 0) {
+        if (lane == 0) run_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0) run_mma<kKind>(p, smem_base, ctrl, tmem_base, abort_flag);
+    } else {
+        run_epilogue<kKind>(p, ctrl, tmem_base, warp, lane, abort_flag);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// A 2-D tiled tensor map with the 128-byte swizzle and zero fill out of range.
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kKind>
+bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, cudaStream_t stream,
+            const DeviceInfo &dev)
+{
+    if (cudaFuncSetAttribute(umma_gemm_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+        return false;
+    const int64_t tiles = p.tiles_m * p.tiles_n;
+    const int64_t grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+    umma_gemm_kernel<kKind><<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
+    return true;
+}
+
+Params make_params(int64_t M, int64_t N, int64_t K, float alpha, float beta, void *C, int64_t ldc,
+                   int bk, bool vec_c)
+{
+    Params p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.ldc = ldc;
+    p.tiles_m = (M + BM - 1) / BM;
+    p.tiles_n = (N + BN - 1) / BN;
+    p.num_kb = (K + bk - 1) / bk;
+    p.vec_c = vec_c ? 1 : 0;
+    return p;
+}
+
+}  // namespace
+
+const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
+                               int64_t lda, const uint16_t *B, int64_t ldb, float beta,
+                               uint16_t *C, int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
+{
+    // TMA needs 16-byte aligned bases and row pitches.
+    if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0) return nullptr;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM))
+        return nullptr;
+    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, BN))
+        return nullptr;
+    const Params p = make_params(M, N, K, alpha, beta, C, ldc, Traits<kF16>::BK,
+                                 aligned16(C) && (ldc % 8 == 0));
+    if (!launch<kF16>(ma, mb, p, stream, dev)) return nullptr;
+    return "umma_f16_tn_128x256x64_tma";
+}
+
+const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                             int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                             int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
+{
+    if (!aligned16(A) || !aligned16(B) || (lda * 4) % 16 != 0 || (ldb * 4) % 16 != 0) return nullptr;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM))
+        return nullptr;
+    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK))
+        return nullptr;
+    const Params p = make_params(M, N, K, alpha, beta, C, ldc, Traits<kTF32>::BK,
+                                 aligned16(C) && (ldc % 4 == 0));
+    if (!launch<kTF32>(ma, mb, p, stream, dev)) return nullptr;
+    return "umma_tf32_128x256x32_tma";
+}
+
+int umma_read_status(int clear)
+{
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_umma_status, sizeof(int)) != cudaSuccess) return DGEMM_ERR_LAUNCH;
+    if (clear) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_umma_status, &zero, sizeof(int)) != cudaSuccess)
+            return DGEMM_ERR_LAUNCH;
+    }
+    return v;
+}
+
+}  // namespace dgemm

@@ -1,0 +1,143 @@
+/*
+ * dgemm.h -- C ABI of libdgemm, a dense row-major GEMM library for one
+ * NVIDIA GB300 (compute capability 10.3, sm_103a).
+ *
+ * Every entry point computes
+ *
+ *     C = alpha * op(A) * op(B) + beta * C
+ *
+ * on the GPU, asynchronously on the caller's CUDA stream, and returns a
+ * dgemm_status.  The operation is the one the pages define:
+ *   - "CUDA GEMM：从基础写法到工程优化", opening definition: C = alpha*A*B +
+ *     beta*C with A (M x K), B (K x N), C (M x N), all row-major;
+ *   - "SGEMM CUDA代码学习", section "问题定义与记号": A[m][k] sits at m*K + k,
+ *     and one output element is one K-long dot product;
+ *   - "Warp Specialization HGEMM", section "6. B 的 RowMajor(K,N) 与 TN 布局":
+ *     the TN layout, where B is stored N x K (row-major) and the product is
+ *     A * B^T.
+ * The pages' matrices are tight (leading dimension = row length); this ABI
+ * adds explicit leading dimensions (lda, ldb, ldc, in elements).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Ownership: the caller owns every buffer.  A and B are device pointers that
+ *   are only read (never modified, not even to round them).  C is a device
+ *   pointer; it is read only when beta != 0 and it is always written (all
+ *   M x N entries, nothing outside them -- padding columns between N and ldc
+ *   are left untouched).
+ * Memory: no call allocates device memory or synchronises; results are
+ *   ready when the stream reaches the call.  The library keeps a per-device
+ *   cache of device properties.
+ * Special cases (BLAS conventions):
+ *   M == 0 or N == 0  -> DGEMM_OK, nothing is launched;
+ *   K == 0 or alpha == 0 -> C = beta * C, A and B are never read; with
+ *                           beta == 0 this writes zeros;
+ *   beta == 0         -> C is never read, so NaN/Inf in it do not propagate.
+ * Validation happens on the host before any launch; an invalid call writes
+ *   nothing and launches nothing.  DGEMM_ERR_INVALID_ARG is returned for
+ *   M, N or K < 0; a leading dimension smaller than its row length
+ *   (lda < K; ldb < N for the NN calls, ldb < K for the TN call; ldc < N);
+ *   a NULL pointer for an operand that would be read or written.
+ * DGEMM_ERR_UNSUPPORTED_DEVICE: the current device is not compute
+ *   capability 10.3.
+ * DGEMM_ERR_LAUNCH: the CUDA runtime reported an error at launch (the
+ *   sticky error state of the context is not cleared).
+ * Aliasing between C and A or B is not supported (results are undefined).
+ * Any alignment is accepted; 16-byte aligned pointers and leading dimensions
+ *   whose byte size is a multiple of 16 take the fastest kernels.
+ * Indexing inside the kernels is 64-bit.
+ */
+#ifndef DGEMM_H
+#define DGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef __CUDA_RUNTIME_API_H__
+struct CUstream_st;
+typedef struct CUstream_st *cudaStream_t;
+#endif
+
+typedef enum {
+    DGEMM_OK = 0,
+    DGEMM_ERR_INVALID_ARG = 1,
+    DGEMM_ERR_UNSUPPORTED_DEVICE = 2,
+    DGEMM_ERR_LAUNCH = 3,
+    DGEMM_ERR_TIMEOUT = 4
+} dgemm_status;
+
+/*
+ * gemm_f32 -- SGEMM on the FP32 pipes (CUDA cores, fused multiply-add in
+ * single precision, round-to-nearest).
+ *   M, N, K : problem size; A is M x K, B is K x N, C is M x N.
+ *   alpha   : scale of the product;  beta: scale of the old C.
+ *   A, lda  : device, float, row-major, element (m, k) at A[m*lda + k].
+ *   B, ldb  : device, float, row-major, element (k, n) at B[k*ldb + n].
+ *   C, ldc  : device, float, row-major, element (m, n) at C[m*ldc + n].
+ *   stream  : CUDA stream (0 = legacy default stream).
+ * Source: "SGEMM CUDA代码学习" (sections "第 1 步" to "第 4 步": block tile,
+ * thread tile, bank-conflict-free staging, double buffering) and
+ * "CUDA GEMM：从基础写法到工程优化" (sections 1 to 12, with alpha/beta).
+ */
+int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha,
+             const float *A, int64_t lda, const float *B, int64_t ldb,
+             float beta, float *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * gemm_tf32 -- same operation, signature and layouts as gemm_f32, but the
+ * products run on the tensor cores in TF32 (each FP32 operand is reduced to
+ * 1+8+10 bits inside the multiplier; the stored A and B are not modified),
+ * with FP32 accumulation and an FP32 alpha/beta epilogue.
+ * Source: "SGEMM CUDA代码学习", section "第 5 步" (TF32 tensor cores: a
+ * 19-bit float, 1+8+10) and its WMMA TF32 multi-stage kernel.
+ */
+int gemm_tf32(int64_t M, int64_t N, int64_t K, float alpha,
+              const float *A, int64_t lda, const float *B, int64_t ldb,
+              float beta, float *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * gemm_f16_tn -- HGEMM in the TN layout: C = alpha * A * B^T + beta * C.
+ *   A, lda  : device, IEEE binary16, M x K row-major, (m, k) at A[m*lda + k].
+ *   B, ldb  : device, IEEE binary16, stored N x K row-major, so the logical
+ *             B(k, n) is B[n*ldb + k] (ldb >= K).
+ *   C, ldc  : device, IEEE binary16, M x N row-major.
+ *   alpha, beta: float.
+ * Products accumulate in FP32 on the tensor cores; alpha*acc + beta*C_old is
+ * formed in FP32 and rounded once to binary16 (round to nearest even;
+ * overflow gives +-Inf).
+ * Source: "HGEMM SMEM Swizzle 代码学习" (FP16 TN tensor-core GEMM with a
+ * swizzled shared-memory layout) and "Warp Specialization HGEMM" (producer /
+ * consumer roles; section "6. B 的 RowMajor(K,N) 与 TN 布局").  The pages
+ * accumulate in FP16; this library accumulates in FP32.
+ */
+int gemm_f16_tn(int64_t M, int64_t N, int64_t K, float alpha,
+                const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                float beta, uint16_t *C, int64_t ldc, cudaStream_t stream);
+
+/* A static, NUL-terminated description of a dgemm_status value. */
+const char *dgemm_status_string(int status);
+
+/*
+ * dgemm_device_status -- read (and, if clear != 0, reset) the current
+ * device's kernel status word.  The tensor-core kernels bound every wait on
+ * an mbarrier; a wait that runs out records DGEMM_ERR_TIMEOUT here and the
+ * kernel exits cleanly instead of hanging.  This call synchronises the
+ * device.  Returns DGEMM_OK when no kernel has recorded an error since the
+ * last clear.  Source: none on the pages (they never check kernels).
+ */
+int dgemm_device_status(int clear);
+
+/*
+ * dgemm_last_kernel -- name of the kernel variant the last successful call
+ * on this host thread launched ("" if none): for tests and the benchmark.
+ */
+const char *dgemm_last_kernel(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGEMM_H */

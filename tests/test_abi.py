@@ -1,0 +1,111 @@
+"""The C-ABI library builds, loads and exports every symbol include/dgemm.h
+declares; host-side validation returns its status before touching a GPU.
+No compute call is made here (these tests run without a GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dgemm.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import dense_gemm_09_gb300 as dg
+    dg.build()
+    return dg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("gemm_f32", "gemm_tf32", "gemm_f16_tn", "dgemm_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    import dense_gemm_09_gb300 as dg
+    out = subprocess.check_output(["nm", "-D", "--defined-only", dg.LIB_PATH], text=True)
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "dgemm.h"\nint main(void){return gemm_f32(0,0,0,1.f,0,0,0,0,0.f,0,0,0);}\n')
+    subprocess.check_call(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           "-c", str(src), "-o", str(tmp_path / "t.o")])
+
+
+def test_status_strings(L):
+    import dense_gemm_09_gb300 as dg
+    for code in range(5):
+        s = dg.status_string(code)
+        assert s.startswith("DGEMM_"), s
+    assert "unknown" in dg.status_string(99)
+
+
+ENTRY = ["gemm_f32", "gemm_tf32", "gemm_f16_tn"]
+P = 0x1000  # a non-null dummy pointer value (never dereferenced: validation fails first)
+
+
+@pytest.mark.parametrize("name", ENTRY)
+@pytest.mark.parametrize("args", [
+    (-1, 8, 8, 1.0, P, 8, P, 8, 0.0, P, 8),      # negative M
+    (8, -1, 8, 1.0, P, 8, P, 8, 0.0, P, 8),      # negative N
+    (8, 8, -1, 1.0, P, 8, P, 8, 0.0, P, 8),      # negative K
+    (8, 8, 8, 1.0, P, 7, P, 8, 0.0, P, 8),       # lda < K
+    (8, 8, 8, 1.0, P, 8, P, 7, 0.0, P, 8),       # ldb < row length of B
+    (8, 8, 8, 1.0, P, 8, P, 8, 0.0, P, 7),       # ldc < N
+    (8, 8, 8, 1.0, 0, 8, P, 8, 0.0, P, 8),       # A null but read
+    (8, 8, 8, 1.0, P, 8, 0, 8, 0.0, P, 8),       # B null but read
+    (8, 8, 8, 1.0, P, 8, P, 8, 0.0, 0, 8),       # C null
+])
+def test_invalid_arguments_rejected_on_host(L, name, args):
+    st = getattr(L, name)(*args, None)
+    assert st == 1  # DGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ENTRY)
+def test_empty_problem_returns_ok_without_device(L, name):
+    assert getattr(L, name)(0, 8, 8, 1.0, 0, 8, 0, 8, 0.0, 0, 8, None) == 0
+    assert getattr(L, name)(8, 0, 8, 1.0, 0, 8, 0, 8, 0.0, 0, 8, None) == 0
+
+
+@pytest.mark.parametrize("name", ENTRY)
+def test_tn_ldb_rule(L, name):
+    # TN: B is N x K, so ldb >= K is the rule (K=16 > N=8 here)
+    st = getattr(L, name)(8, 8, 16, 1.0, P, 16, P, 8, 0.0, P, 8, None)
+    if name == "gemm_f16_tn":
+        assert st == 1
+    else:
+        assert st != 1  # ldb = N = 8 is valid for the NN calls
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+@pytest.mark.parametrize("name", ENTRY)
+def test_no_gpu_reports_unsupported_device(L, name):
+    assert getattr(L, name)(8, 8, 8, 1.0, P, 8, P, 8, 0.0, P, 8, None) == 2
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import dense_gemm_09_gb300 as dg
+    monkeypatch.setattr(dg, "_lib", None)
+    monkeypatch.setattr(dg, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        dg.lib()
+
+
+def test_last_kernel_empty_before_any_launch(L):
+    assert L.dgemm_last_kernel() == b""

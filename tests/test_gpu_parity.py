@@ -1,0 +1,180 @@
+"""Parity of the CUDA paths (through the C ABI) with the CPU oracle.
+
+Small and ragged shapes are compared in full, element by element, against
+the acceptance rule |C_gpu - ref| <= tol*(|A||B|)_ij + tol*|beta*c_ij| with
+tol = 1e-6*sqrt(K) (FP32), 2e-3 (TF32), 1e-3 (FP16 -> FP32).  Small-integer
+operands make every path exact, so those cases are compared bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import dense_gemm_09_gb300 as dg
+    dg.lib()
+    dg.device_status(clear=True)
+    yield dg
+    assert dg.device_status(clear=True) == dg.OK
+
+
+# Shapes: tiny, tile-exact, ragged in every dimension, several tiles, and a
+# tile count above the SM count (persistent CTAs take several tiles).
+SHAPES = {
+    "f32": [(1, 1, 1), (5, 7, 3), (17, 9, 33), (31, 33, 32), (128, 128, 16), (129, 127, 17),
+            (255, 257, 300), (300, 520, 1000), (1, 300, 700), (700, 1, 300), (64, 1000, 5)],
+    "tf32": [(1, 4, 4), (5, 8, 12), (17, 12, 36), (128, 256, 32), (129, 260, 36), (255, 516, 300),
+             (300, 520, 1000), (1, 300, 704), (700, 4, 300), (64, 1000, 8)],
+    "f16_tn": [(1, 1, 8), (5, 7, 16), (17, 9, 40), (128, 256, 64), (129, 257, 72), (255, 513, 304),
+               (300, 520, 1000), (1, 300, 704), (700, 1, 304), (64, 1000, 8)],
+}
+
+
+@pytest.mark.parametrize("path,shape", [(p, s) for p in parity.PATHS for s in SHAPES[p]])
+def test_random_shapes_full(path, shape):
+    M, N, K = shape
+    A, B, C = parity.host_operands(path, M, N, K, seed=M + 7 * N + 13 * K)
+    got, _, _ = parity.run(path, A, B, C, 1.5, -0.25)
+    assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+@pytest.mark.parametrize("path", parity.PATHS)
+def test_beta_zero_alpha_one(path):
+    M, N, K = 200, 264, 136
+    A, B, C = parity.host_operands(path, M, N, K, seed=3)
+    got, _, _ = parity.run(path, A, B, C, 1.0, 0.0)
+    assert parity.worst_ratio(path, got, A, B, C, 1.0, 0.0) <= 1.0
+
+
+@pytest.mark.parametrize("path,shape", [
+    ("f32", (64, 72, 300)), ("f32", (129, 257, 1000)),
+    ("tf32", (64, 72, 300)), ("tf32", (129, 260, 1000)),
+    ("f16_tn", (64, 72, 304)), ("f16_tn", (129, 257, 1024))])
+def test_small_integers_bit_exact(path, shape):
+    # every partial sum is an integer below 2^24: any summation order is exact
+    M, N, K = shape
+    A, B, C = parity.host_operands(path, M, N, K, seed=11, dist="int")
+    beta = 2.0 if path != "f16_tn" else 1.0
+    got, _, _ = parity.run(path, A, B, C, 1.0, beta)
+    ref, _ = parity.reference(path, A, B, C, 1.0, beta)
+    assert np.array_equal(got.numpy().astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("path", parity.PATHS)
+def test_identity_and_permutation_exact(path):
+    M = 136
+    N = 264
+    g = si.generator(5)
+    dt = torch.float16 if path == "f16_tn" else torch.float32
+    perm = torch.randperm(M, generator=g)
+    P = torch.zeros((M, M), dtype=dt)
+    P[torch.arange(M), perm] = 1
+    Bl = si.uniform((M, N), g).to(dt)          # logical B (K x N)
+    B = Bl.T.contiguous() if path == "f16_tn" else Bl
+    C = torch.zeros((M, N), dtype=dt)
+    got, _, _ = parity.run(path, P, B, C, 1.0, 0.0)
+    want = Bl[perm]
+    if path == "tf32":
+        # the product reads B through TF32: compare with the oracle's exact values
+        ref, _ = parity.reference(path, P, B, C, 1.0, 0.0)
+        assert np.array_equal(got.numpy().astype(np.float64), ref)
+    else:
+        assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("path", parity.PATHS)
+def test_alpha_zero_does_not_read_a_b(path):
+    M, N, K = 70, 136, 64
+    A, B, C = parity.host_operands(path, M, N, K, seed=2)
+    A = torch.full_like(A, float("nan"))
+    B = torch.full_like(B, float("nan"))
+    got, _, _ = parity.run(path, A, B, C, 0.0, 0.5)
+    want = (C.double() * 0.5)
+    assert torch.equal(got.double(), want.to(got.dtype).double())
+
+
+@pytest.mark.parametrize("path", parity.PATHS)
+def test_beta_zero_does_not_read_c(path):
+    M, N, K = 70, 136, 64
+    A, B, C = parity.host_operands(path, M, N, K, seed=4)
+    Cnan = torch.full_like(C, float("nan"))
+    got, _, _ = parity.run(path, A, B, Cnan, 1.0, 0.0)
+    assert torch.isfinite(got).all()
+    assert parity.worst_ratio(path, got, A, B, C, 1.0, 0.0) <= 1.0
+
+
+@pytest.mark.parametrize("path", parity.PATHS)
+def test_k_zero_scales_c(path):
+    M, N = 33, 40
+    _, _, C = parity.host_operands(path, M, N, 8, seed=6)
+    A = torch.zeros((M, 0), dtype=C.dtype)
+    B = torch.zeros((0, N) if path != "f16_tn" else (N, 0), dtype=C.dtype)
+    got, _, _ = parity.run(path, A, B, C, 1.0, -2.0)
+    assert torch.equal(got, (C.double() * -2.0).to(C.dtype))
+    got, _, _ = parity.run(path, A, B, C, 1.0, 0.0)
+    assert torch.equal(got, torch.zeros_like(C))
+
+
+@pytest.mark.parametrize("path", parity.PATHS)
+def test_empty_m_or_n_is_a_no_op(path):
+    import dense_gemm_09_gb300 as dg
+    dt = torch.float16 if path == "f16_tn" else torch.float32
+    fn = {"f32": dg.gemm_f32, "tf32": dg.gemm_tf32, "f16_tn": dg.gemm_f16_tn}[path]
+    for M, N in ((0, 16), (16, 0)):
+        A = torch.ones((M, 8), dtype=dt, device="cuda")
+        B = torch.ones((8, N) if path != "f16_tn" else (N, 8), dtype=dt, device="cuda")
+        C = torch.ones((M, N), dtype=dt, device="cuda")
+        fn(A, B, C, 1.0, 1.0)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("path", parity.PATHS)
+def test_padded_leading_dims_and_canaries(path):
+    # C lives in a wider buffer filled with NaN; only the M x N entries change
+    M, N, K = 150, 264, 200
+    A, B, C = parity.host_operands(path, M, N, K, seed=8)
+    pad = (8, 8, 32)  # keeps 16-byte row pitches for every path
+    got, dC, cbuf = parity.run(path, A, B, C, 1.0, 0.5, pad=pad)
+    assert parity.worst_ratio(path, got, A, B, C, 1.0, 0.5) <= 1.0
+    ld = N + pad[2]
+    rows = cbuf[:M * ld].view(M, ld)
+    assert torch.isnan(rows[:, N:]).all()          # padding columns untouched
+    assert torch.isnan(cbuf[M * ld:]).all()        # rows past M untouched
+
+
+def test_f32_unaligned_leading_dims():
+    # odd pitches and a base pointer off a 16-byte boundary: scalar-load path
+    M, N, K = 131, 133, 137
+    A, B, C = parity.host_operands("f32", M, N, K, seed=9)
+    got, _, _ = parity.run("f32", A, B, C, 1.5, -0.25, pad=(1, 3, 1), offset=(1, 2, 3))
+    assert parity.worst_ratio("f32", got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
+def test_many_tiles_per_cta(path):
+    # more tiles than SMs: each persistent CTA runs several tiles and both
+    # TMEM accumulators
+    M, N, K = 2048, 4096, 192
+    A, B, C = parity.host_operands(path, M, N, K, seed=10)
+    got, dC, _ = parity.run(path, A, B, C, 1.0, 0.5)
+    assert parity.sampled_check(path, dC, A, B, C, 1.0, 0.5) <= 1.0
+
+
+def test_stream_argument_is_honoured():
+    import dense_gemm_09_gb300 as dg
+    s = torch.cuda.Stream()
+    A, B, C = parity.host_operands("f32", 256, 256, 256, seed=12)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        dg.gemm_f32(dA, dB, dC, 1.0, 1.0, stream=s)
+    s.synchronize()
+    assert parity.worst_ratio("f32", dC.cpu(), A, B, C, 1.0, 1.0) <= 1.0
