@@ -178,20 +178,26 @@ __device__ __forceinline__ void tmem_ld_wait()
 
 // ---------------------------------------------------------------- descriptors
 
-// Shared-memory matrix descriptor for tcgen05.mma with the 128-byte swizzle
-// (layout code 2 in bits 61-63; bits 46-47 carry the fixed value 1).  Start
-// address, leading-dimension and stride-dimension byte offsets are stored in
-// 16-byte units.  The swizzle pattern is anchored at 1024-byte boundaries, so
-// every tile base handed to this must be 1024-byte aligned (base offset 0).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes,
-                                               uint32_t sbo_bytes)
+// Shared-memory matrix descriptor for tcgen05.mma.  Start address, leading-
+// and stride-dimension byte offsets are stored in 16-byte units; bits 46-47
+// carry the fixed value 1; bits 61-63 the swizzle layout:
+//   kSw128     (2): 128-byte swizzle of 16-byte chunks, 8 rows x 128 B atoms;
+//   kSw128A32  (1): 128-byte swizzle of 32-byte chunks (the layout the MMA
+//                   reads for N-major 32-bit operands).
+// The swizzle pattern is anchored at 1024-byte boundaries, so every tile base
+// handed to this must be 1024-byte aligned (base offset 0).
+constexpr uint32_t kSw128 = 2;
+constexpr uint32_t kSw128A32 = 1;
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes, uint32_t layout)
 {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= 1ull << 46;
-    d |= 2ull << 61;
+    d |= static_cast<uint64_t>(layout & 7u) << 61;
     return d;
 }
 

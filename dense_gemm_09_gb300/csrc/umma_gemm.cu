@@ -188,8 +188,8 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
             if constexpr (kKind == kF16) {
                 ptx::tma_load_2d(sb, tmap_b, full, kc, static_cast<int32_t>(n0));
             } else {
-                // B is N-major: eight 32(N) x 32(K) boxes, one 4 KB swizzle
-                // column each.
+                // B is N-major: eight 32(N) x 32(K) boxes, one 4 KB column
+                // each, written with the 32-byte-atom 128-byte swizzle.
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c)
                     ptx::tma_load_2d(sb + c * 4096, tmap_b, full,
@@ -236,13 +236,18 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
             const uint32_t sb = sa + A_TILE_BYTES;
 #pragma unroll
             for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
-                // A (K-major): advance 32 bytes along the swizzled row.
-                const uint64_t da = ptx::sw128_desc(sa + k * 32, 16, 1024);
+                // A (K-major): advance 32 bytes along the swizzled row; 8-row
+                // groups of the tile are 1024 bytes apart.
+                const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
                 uint64_t db;
-                if constexpr (kKind == kF16)
-                    db = ptx::sw128_desc(sb + k * 32, 16, 1024);
-                else  // B (N-major): next 8 K-rows; 4 KB between 32-wide N columns
-                    db = ptx::sw128_desc(sb + k * 1024, 4096, 1024);
+                if constexpr (kKind == kF16) {
+                    db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
+                } else {
+                    // B (N-major, 32-byte swizzle atoms): one MMA covers 8 K-rows
+                    // (1 KB), read as two 4-row groups 512 B apart; 32-wide N
+                    // columns are 4 KB apart.
+                    db = ptx::smem_desc(sb + k * 1024, 4096, 512, ptx::kSw128A32);
+                }
                 ptx::umma<kKind>(d_tmem, da, db, T::kIdesc, (kb | k) != 0 ? 1u : 0u);
             }
             ptx::umma_commit(ptx::smem_addr(&ctrl->empty[stage]));
@@ -442,9 +447,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-// A 2-D tiled tensor map with the 128-byte swizzle and zero fill out of range.
+// A 2-D tiled tensor map with a 128-byte swizzle and zero fill out of range.
 bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
-              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer)
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swizzle)
 {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
@@ -453,7 +459,7 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -498,9 +504,11 @@ const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, con
     // TMA needs 16-byte aligned bases and row pitches.
     if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0) return nullptr;
     CUtensorMap ma, mb;
-    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM))
+    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return nullptr;
-    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, BN))
+    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, BN,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return nullptr;
     const Params p = make_params(M, N, K, alpha, beta, C, ldc, Traits<kF16>::BK,
                                  aligned16(C) && (ldc % 8 == 0));
@@ -514,9 +522,11 @@ const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const
 {
     if (!aligned16(A) || !aligned16(B) || (lda * 4) % 16 != 0 || (ldb * 4) % 16 != 0) return nullptr;
     CUtensorMap ma, mb;
-    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM))
+    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return nullptr;
-    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK))
+    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK,
+                  CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B))
         return nullptr;
     const Params p = make_params(M, N, K, alpha, beta, C, ldc, Traits<kTF32>::BK,
                                  aligned16(C) && (ldc % 4 == 0));

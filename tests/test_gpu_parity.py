@@ -178,3 +178,22 @@ def test_stream_argument_is_honoured():
         dg.gemm_f32(dA, dB, dC, 1.0, 1.0, stream=s)
     s.synchronize()
     assert parity.worst_ratio("f32", dC.cpu(), A, B, C, 1.0, 1.0) <= 1.0
+
+
+def test_tf32_operand_rounding_is_truncation():
+    # Crafted operands decide how FP32 values are reduced to TF32 inside the
+    # multiplier: 1+2^-11 is a tie (nearest-away gives 1+2^-10), 1+2^-11+2^-13
+    # is above the tie (any nearest mode gives 1+2^-10).  Truncation keeps 1.
+    import dense_gemm_09_gb300 as dg
+    xs = [1 + 2**-11, 1 + 2**-11 + 2**-13, 1 + 2**-12, -(1 + 2**-11), 1 + 3 * 2**-11, 3.0]
+    K = 8
+    A = torch.zeros((len(xs), K))
+    A[:, 0] = torch.tensor(xs)
+    B = torch.zeros((K, 8))
+    B[0, :] = 1.0
+    C = torch.zeros((len(xs), 8))
+    got, _, _ = parity.run("tf32", A, B, C, 1.0, 0.0)
+    want = [1.0, 1.0, 1.0, -1.0, 1 + 2**-10, 3.0]
+    assert got[:, 0].tolist() == want
+    ref, _ = parity.reference("tf32", A, B, C, 1.0, 0.0)
+    assert np.array_equal(got.numpy().astype(np.float64), ref)
