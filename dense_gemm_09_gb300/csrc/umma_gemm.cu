@@ -41,6 +41,7 @@
 // own copies and MMAs in flight, and the CTA releases its TMEM and exits.
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -60,7 +61,6 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int STAGES = 4;
-constexpr int THREADS = 192;
 constexpr int ROW_BYTES = 128;                     // one swizzled row
 constexpr int A_TILE_BYTES = BM * ROW_BYTES;       // 16 KB
 constexpr int B_TILE_BYTES = BN * ROW_BYTES;       // 32 KB
@@ -82,6 +82,7 @@ struct Traits<kF16> {
     // D = f32 (bits 4-5 = 1), A = B = f16 (0), both K-major, N >> 3, M >> 4.
     static constexpr uint32_t kIdesc =
         (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+    static constexpr uint32_t kIdescKMajorB = kIdesc;
 };
 template <>
 struct Traits<kTF32> {
@@ -92,6 +93,8 @@ struct Traits<kTF32> {
     static constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (1u << 16) |
                                        (static_cast<uint32_t>(BN >> 3) << 17) |
                                        (static_cast<uint32_t>(BM >> 4) << 24);
+    // B staged K-major (the register-path producer transposes it).
+    static constexpr uint32_t kIdescKMajorB = kIdesc & ~(1u << 16);
 };
 
 struct Ctrl {
@@ -113,6 +116,10 @@ struct Params {
     int64_t ldc;
     int64_t tiles_m, tiles_n, num_kb;
     int vec_c;
+    // operands for the register-path producer (unused with TMA)
+    const void *A;
+    const void *B;
+    int64_t lda, ldb;
 };
 
 __device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t &m0, int64_t &n0)
@@ -211,7 +218,98 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
     }
 }
 
+// Byte offset of (row r, byte b of the row) in a K-major tile of 128-byte
+// rows under the 128-byte swizzle: 16-byte chunk j of row r is stored at
+// chunk position j ^ (r mod 8).  This is the placement TMA's 128-byte swizzle
+// writes, so both producers feed the same MMA descriptors.
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t b)
+{
+    return r * 128u + ((((b >> 4) ^ (r & 7u)) << 4) | (b & 15u));
+}
+
+template <typename E>
+__device__ __forceinline__ void st_shared(uint32_t addr, E v)
+{
+    if constexpr (sizeof(E) == 2)
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+    else
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Register-path producer for operands TMA cannot describe (base pointers or
+// row pitches that are not 16-byte aligned): 128 threads load elements with
+// plain predicated loads (zeros outside M, N, K), write them into the same
+// swizzled K-major tiles -- transposing an N-major B on the way -- then make
+// the writes visible to the tensor core (proxy fence) and arrive on the
+// stage's "full" barrier (128 arrivals).
 template <int kKind>
+__device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_base, Ctrl *ctrl,
+                                                 int ptid, volatile int *abort_flag)
+{
+    using T = Traits<kKind>;
+    using E = typename std::conditional<kKind == kF16, uint16_t, uint32_t>::type;
+    constexpr int BK = T::BK;
+    constexpr int kBatch = 8;
+    const E *__restrict__ A = static_cast<const E *>(p.A);
+    const E *__restrict__ B = static_cast<const E *>(p.B);
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    uint32_t stage = 0, phase = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int64_t m0, n0;
+        tile_coords(t, p, m0, n0);
+        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, abort_flag)) return;
+            const int64_t k0 = kb * BK;
+            const uint32_t sa = smem_base + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_TILE_BYTES;
+            // A tile: BM rows x BK; consecutive threads take consecutive k.
+            for (int i0 = 0; i0 < BM * BK / 128; i0 += kBatch) {
+                E v[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int idx = ptid + (i0 + u) * 128;
+                    const int64_t gm = m0 + idx / BK, gk = k0 + idx % BK;
+                    v[u] = (gm < p.M && gk < p.K) ? A[gm * p.lda + gk] : E(0);
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int idx = ptid + (i0 + u) * 128;
+                    st_shared(sa + sw128_offset(idx / BK, (idx % BK) * sizeof(E)), v[u]);
+                }
+            }
+            // B tile, staged K-major: row n holds BK consecutive k.
+            for (int i0 = 0; i0 < BN * BK / 128; i0 += kBatch) {
+                E v[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int idx = ptid + (i0 + u) * 128;
+                    if constexpr (kKind == kF16) {  // B stored N x K: walk k
+                        const int64_t gn = n0 + idx / BK, gk = k0 + idx % BK;
+                        v[u] = (gn < p.N && gk < p.K) ? B[gn * p.ldb + gk] : E(0);
+                    } else {  // B stored K x N: walk n (coalesced), transpose into smem
+                        const int64_t gn = n0 + idx % BN, gk = k0 + idx / BN;
+                        v[u] = (gn < p.N && gk < p.K) ? B[gk * p.ldb + gn] : E(0);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int idx = ptid + (i0 + u) * 128;
+                    const int n = (kKind == kF16) ? idx / BK : idx % BN;
+                    const int k = (kKind == kF16) ? idx % BK : idx / BN;
+                    st_shared(sb + sw128_offset(n, k * sizeof(E)), v[u]);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(ptx::smem_addr(&ctrl->full[stage]));
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+template <int kKind, bool kTma>
 __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctrl *ctrl,
                                         uint32_t tmem_base, volatile int *abort_flag)
 {
@@ -240,7 +338,8 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
                 // groups of the tile are 1024 bytes apart.
                 const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
                 uint64_t db;
-                if constexpr (kKind == kF16) {
+                if constexpr (kKind == kF16 || !kTma) {
+                    // B staged K-major like A
                     db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
                 } else {
                     // B (N-major, 32-byte swizzle atoms): one MMA covers 8 K-rows
@@ -248,7 +347,8 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
                     // columns are 4 KB apart.
                     db = ptx::smem_desc(sb + k * 1024, 4096, 512, ptx::kSw128A32);
                 }
-                ptx::umma<kKind>(d_tmem, da, db, T::kIdesc, (kb | k) != 0 ? 1u : 0u);
+                ptx::umma<kKind>(d_tmem, da, db, kTma ? T::kIdesc : T::kIdescKMajorB,
+                                 (kb | k) != 0 ? 1u : 0u);
             }
             ptx::umma_commit(ptx::smem_addr(&ctrl->empty[stage]));
             if (++stage == STAGES) {
@@ -374,11 +474,24 @@ __device__ __forceinline__ void run_epilogue(const Params &p, Ctrl *ctrl, uint32
     }
 }
 
-template <int kKind>
-__global__ void __launch_bounds__(THREADS, 1)
+// Threads per CTA: producer warp(s), one MMA warp, four epilogue warps.
+template <bool kTma>
+constexpr int producer_warps()
+{
+    return kTma ? 1 : 4;
+}
+template <bool kTma>
+constexpr int cta_threads()
+{
+    return 32 * (producer_warps<kTma>() + 1 + 4);
+}
+
+template <int kKind, bool kTma>
+__global__ void __launch_bounds__(cta_threads<kTma>(), 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b, const Params p)
 {
+    constexpr int kMmaWarp = producer_warps<kTma>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -387,7 +500,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(ptx::smem_addr(&ctrl->full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctrl->full[s]), kTma ? 1 : 32 * producer_warps<kTma>());
             ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -398,11 +511,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         ctrl->abort = 0;
         ptx::fence_mbarrier_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (kTma && warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmap_a);
         ptx::prefetch_tmap(&tmap_b);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_addr(&ctrl->tmem_base), TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -413,17 +526,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int *abort_flag = &ctrl->abort;
     const uint32_t smem_base = ptx::smem_addr(smem);
 
-    if (warp == 0) {
-        if (lane == 0) run_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, abort_flag);
-    } else if (warp == 1) {
-        if (lane == 0) run_mma<kKind>(p, smem_base, ctrl, tmem_base, abort_flag);
+    if (warp < kMmaWarp) {
+        if constexpr (kTma) {
+            if (lane == 0) run_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, abort_flag);
+        } else {
+            run_reg_producer<kKind>(p, smem_base, ctrl, threadIdx.x, abort_flag);
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) run_mma<kKind, kTma>(p, smem_base, ctrl, tmem_base, abort_flag);
     } else {
         run_epilogue<kKind>(p, ctrl, tmem_base, warp, lane, abort_flag);
     }
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, TMEM_COLS);
@@ -464,21 +581,22 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kKind>
+template <int kKind, bool kTma>
 bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, cudaStream_t stream,
             const DeviceInfo &dev)
 {
-    if (cudaFuncSetAttribute(umma_gemm_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(umma_gemm_kernel<kKind, kTma>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
         return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
     const int64_t grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-    umma_gemm_kernel<kKind><<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
+    umma_gemm_kernel<kKind, kTma>
+        <<<static_cast<unsigned>(grid), cta_threads<kTma>(), SMEM_BYTES, stream>>>(ma, mb, p);
     return true;
 }
 
-Params make_params(int64_t M, int64_t N, int64_t K, float alpha, float beta, void *C, int64_t ldc,
-                   int bk, bool vec_c)
+Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                   const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int bk, bool vec_c)
 {
     Params p;
     p.M = M;
@@ -492,6 +610,10 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, float beta, voi
     p.tiles_n = (N + BN - 1) / BN;
     p.num_kb = (K + bk - 1) / bk;
     p.vec_c = vec_c ? 1 : 0;
+    p.A = A;
+    p.B = B;
+    p.lda = lda;
+    p.ldb = ldb;
     return p;
 }
 
@@ -501,37 +623,35 @@ const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, con
                                int64_t lda, const uint16_t *B, int64_t ldb, float beta,
                                uint16_t *C, int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
 {
-    // TMA needs 16-byte aligned bases and row pitches.
-    if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0) return nullptr;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
-        return nullptr;
-    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, BN,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
-        return nullptr;
-    const Params p = make_params(M, N, K, alpha, beta, C, ldc, Traits<kF16>::BK,
+    const Params p = make_params(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, Traits<kF16>::BK,
                                  aligned16(C) && (ldc % 8 == 0));
-    if (!launch<kF16>(ma, mb, p, stream, dev)) return nullptr;
-    return "umma_f16_tn_128x256x64_tma";
+    // TMA needs 16-byte aligned bases and row pitches.
+    const bool tma = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
+    CUtensorMap ma{}, mb{};
+    if (tma && make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+        make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, BN,
+                 CU_TENSOR_MAP_SWIZZLE_128B)) {
+        return launch<kF16, true>(ma, mb, p, stream, dev) ? "umma_f16_tn_128x256x64_tma" : nullptr;
+    }
+    return launch<kF16, false>(ma, mb, p, stream, dev) ? "umma_f16_tn_128x256x64_ldst" : nullptr;
 }
 
 const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                              int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                              int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
 {
-    if (!aligned16(A) || !aligned16(B) || (lda * 4) % 16 != 0 || (ldb * 4) % 16 != 0) return nullptr;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
-        return nullptr;
-    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK,
-                  CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B))
-        return nullptr;
-    const Params p = make_params(M, N, K, alpha, beta, C, ldc, Traits<kTF32>::BK,
+    const Params p = make_params(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, Traits<kTF32>::BK,
                                  aligned16(C) && (ldc % 4 == 0));
-    if (!launch<kTF32>(ma, mb, p, stream, dev)) return nullptr;
-    return "umma_tf32_128x256x32_tma";
+    const bool tma = aligned16(A) && aligned16(B) && (lda * 4) % 16 == 0 && (ldb * 4) % 16 == 0;
+    CUtensorMap ma{}, mb{};
+    if (tma && make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+        make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK,
+                 CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)) {
+        return launch<kTF32, true>(ma, mb, p, stream, dev) ? "umma_tf32_128x256x32_tma" : nullptr;
+    }
+    return launch<kTF32, false>(ma, mb, p, stream, dev) ? "umma_tf32_128x256x32_ldst" : nullptr;
 }
 
 int umma_read_status(int clear)

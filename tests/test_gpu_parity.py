@@ -31,10 +31,14 @@ def _lib():
 SHAPES = {
     "f32": [(1, 1, 1), (5, 7, 3), (17, 9, 33), (31, 33, 32), (128, 128, 16), (129, 127, 17),
             (255, 257, 300), (300, 520, 1000), (1, 300, 700), (700, 1, 300), (64, 1000, 5)],
+    # TF32 / FP16: 16-byte multiples of the row pitch take the TMA producer,
+    # the others (odd K for A, odd N for TF32's B) the register-path producer
     "tf32": [(1, 4, 4), (5, 8, 12), (17, 12, 36), (128, 256, 32), (129, 260, 36), (255, 516, 300),
-             (300, 520, 1000), (1, 300, 704), (700, 4, 300), (64, 1000, 8)],
+             (300, 520, 1000), (1, 300, 704), (700, 4, 300), (64, 1000, 8),
+             (1, 1, 1), (5, 7, 3), (17, 9, 33), (129, 127, 17), (255, 257, 301)],
     "f16_tn": [(1, 1, 8), (5, 7, 16), (17, 9, 40), (128, 256, 64), (129, 257, 72), (255, 513, 304),
-               (300, 520, 1000), (1, 300, 704), (700, 1, 304), (64, 1000, 8)],
+               (300, 520, 1000), (1, 300, 704), (700, 1, 304), (64, 1000, 8),
+               (1, 1, 1), (5, 7, 3), (17, 9, 33), (129, 127, 17), (255, 257, 301)],
 }
 
 
@@ -197,3 +201,40 @@ def test_tf32_operand_rounding_is_truncation():
     assert got[:, 0].tolist() == want
     ref, _ = parity.reference("tf32", A, B, C, 1.0, 0.0)
     assert np.array_equal(got.numpy().astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
+@pytest.mark.parametrize("shape,pad,offset", [
+    ((131, 133, 137), (1, 3, 1), (1, 2, 3)),      # odd pitches, misaligned bases
+    ((300, 520, 256), (1, 0, 0), (0, 0, 0)),      # only A's pitch is odd
+    ((300, 520, 256), (0, 1, 0), (0, 0, 0)),      # only B's pitch is odd
+    ((300, 520, 256), (0, 0, 0), (2, 0, 0)),      # only A's base is off 16 bytes
+    ((700, 1030, 515), (3, 5, 7), (1, 1, 1)),     # several tiles per CTA
+])
+def test_tensor_paths_register_producer(path, shape, pad, offset):
+    import dense_gemm_09_gb300 as dg
+    M, N, K = shape
+    A, B, C = parity.host_operands(path, M, N, K, seed=M + N + K)
+    got, _, _ = parity.run(path, A, B, C, 1.5, -0.25, pad=pad, offset=offset)
+    assert dg.last_kernel().endswith("_ldst")
+    assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
+def test_register_producer_integers_bit_exact(path):
+    M, N, K = 257, 300, 259
+    A, B, C = parity.host_operands(path, M, N, K, seed=21, dist="int")
+    got, _, _ = parity.run(path, A, B, C, 1.0, 1.0)
+    ref, _ = parity.reference(path, A, B, C, 1.0, 1.0)
+    assert np.array_equal(got.numpy().astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("path", parity.PATHS)
+def test_kernel_variant_names(path):
+    import dense_gemm_09_gb300 as dg
+    A, B, C = parity.host_operands(path, 256, 256, 256, seed=1)
+    parity.run(path, A, B, C, 1.0, 0.0)
+    want = {"f32": "sgemm_simt", "tf32": "umma_tf32", "f16_tn": "umma_f16_tn"}[path]
+    assert dg.last_kernel().startswith(want)
+    if path != "f32":
+        assert dg.last_kernel().endswith("_tma")
