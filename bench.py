@@ -24,7 +24,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -141,15 +140,16 @@ def _max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def _traffic_for(kernel_file: str, kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, only if the
-    kernel source has not changed since the counters were taken."""
+def _traffic_for(kernel_file: str, kernel_key: str, shape):
+    """DRAM bytes per launch from the committed ncu summary for this kernel
+    and shape, only if the kernel source has not changed since the counters
+    were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    e = d.get(kernel_key)
+    e = d.get("%s@%dx%dx%d" % ((kernel_key,) + tuple(shape)))
     if not e:
         return None
     src = os.path.join(ROOT, "dense_gemm_09_gb300", "csrc", kernel_file)
@@ -172,30 +172,36 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     dg.lib()
     stream = torch.cuda.current_stream()
+    Mx, Nx, Kx = args.shape
+    flops = 2.0 * Mx * Nx * Kx
+    paths_run = args.paths
 
     # operands: one seeded problem per rank (replicas, weak scaling)
-    w32 = si.WORKLOADS["f32_8192x8192x4096"]
-    w16 = si.WORKLOADS["f16_tn_8192x8192x4096"]
-    A32h, B32h, _ = si.make(w32, seed=rank, pin=True)
-    A16h, B16h, _ = si.make(w16, seed=rank, pin=True)
-    A32, B32 = A32h.to(dev), B32h.to(dev)
-    A16, B16 = A16h.to(dev), B16h.to(dev)
-    C32 = torch.zeros((M, N), dtype=torch.float32, device=dev)
-    C16 = torch.zeros((M, N), dtype=torch.float16, device=dev)
+    ops = {}
+    if any(p in ("f32_simt", "tf32") for p in paths_run):
+        w = si.Workload("bench_f32", "f32", Mx, Nx, Kx, 1.0, 0.0, "uniform", c_zero=True)
+        Ah, Bh, _ = si.make(w, seed=rank, pin=True)
+        f32 = (Ah, Bh, Ah.to(dev), Bh.to(dev), torch.zeros((Mx, Nx), dtype=torch.float32, device=dev))
+        ops["f32_simt"] = ops["tf32"] = f32
+    if "f16_tn" in paths_run:
+        w = si.Workload("bench_f16", "f16_tn", Mx, Nx, Kx, 1.0, 0.0, "normal_sqrtk", c_zero=True)
+        Ah, Bh, _ = si.make(w, seed=rank, pin=True)
+        ops["f16_tn"] = (Ah, Bh, Ah.to(dev), Bh.to(dev),
+                         torch.zeros((Mx, Nx), dtype=torch.float16, device=dev))
+    fns = {"f32_simt": dg.gemm_f32, "tf32": dg.gemm_tf32, "f16_tn": dg.gemm_f16_tn}
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    calls = {
-        "f32_simt": lambda: dg.gemm_f32(A32, B32, C32, 1.0, 0.0, stream=stream),
-        "tf32": lambda: dg.gemm_tf32(A32, B32, C32, 1.0, 0.0, stream=stream),
-        "f16_tn": lambda: dg.gemm_f16_tn(A16, B16, C16, 1.0, 0.0, stream=stream),
-    }
     kernels = {}
 
+    def call(p):
+        _, _, Ad, Bd, Cd = ops[p]
+        fns[p](Ad, Bd, Cd, 1.0, 0.0, stream=stream)
+
     def step(record):
-        for p in PATHS:
+        for p in paths_run:
             flush.zero_()
             if record is not None:
                 record[p][0].record(stream)
-            calls[p]()
+            call(p)
             if record is not None:
                 record[p][1].record(stream)
             kernels[p] = dg.last_kernel()
@@ -205,7 +211,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     events = [{p: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for p in PATHS} for _ in range(args.steps)]
+               for p in paths_run} for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -216,53 +222,56 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     per_path = {p: [events[s][p][0].elapsed_time(events[s][p][1]) for s in range(args.steps)]
-                for p in PATHS}
+                for p in paths_run}
     ms_step_local = sum(statistics.mean(v) for v in per_path.values())
     ms_step = _max_over_ranks(ms_step_local, world, dev)
-    total_flops = 3 * FLOPS * world
+    total_flops = len(paths_run) * flops * world
     value = total_flops / (ms_step * 1e-3) / 1e12
 
     # ---- end to end through the public API, operands in pinned host memory
-    C32h = torch.empty((M, N), dtype=torch.float32).pin_memory()
-    C16h = torch.empty((M, N), dtype=torch.float16).pin_memory()
-    h2d = 2 * (A32h.numel() * 4 + B32h.numel() * 4) + A16h.numel() * 2 + B16h.numel() * 2
-    d2h = 2 * C32h.numel() * 4 + C16h.numel() * 2
+    e2e = None
+    if not args.no_e2e:
+        hosts_c = {p: torch.empty((Mx, Nx), dtype=ops[p][4].dtype).pin_memory() for p in paths_run}
+        h2d = sum(ops[p][0].numel() * ops[p][0].element_size() + ops[p][1].numel() * ops[p][1].element_size()
+                  for p in paths_run)
+        d2h = sum(hosts_c[p].numel() * hosts_c[p].element_size() for p in paths_run)
 
-    def e2e_step():
-        for p, (Ah, Bh, Ad, Bd, Cd, Ch) in (
-                ("f32_simt", (A32h, B32h, A32, B32, C32, C32h)),
-                ("tf32", (A32h, B32h, A32, B32, C32, C32h)),
-                ("f16_tn", (A16h, B16h, A16, B16, C16, C16h))):
-            Ad.copy_(Ah, non_blocking=True)
-            Bd.copy_(Bh, non_blocking=True)
-            calls[p]()
-            Ch.copy_(Cd, non_blocking=True)
+        def e2e_step():
+            for p in paths_run:
+                Ah, Bh, Ad, Bd, Cd = ops[p]
+                Ad.copy_(Ah, non_blocking=True)
+                Bd.copy_(Bh, non_blocking=True)
+                call(p)
+                hosts_c[p].copy_(Cd, non_blocking=True)
 
-    e2e_steps = max(1, min(args.steps, 5))
-    e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
+        e2e_steps = max(1, min(args.steps, 5))
         e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
-    e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+        e2e = {"value": round(total_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4),
+               "how": "per path: pinned host A, B -> device, the C-ABI call, C -> pinned host"}
     assert dg.device_status() == dg.OK
 
     peaks = _peaks()
     paths = {}
-    for p in PATHS:
+    for p in paths_run:
         ms = statistics.mean(per_path[p])
-        tf = FLOPS / (ms * 1e-3) / 1e12
+        tf = flops / (ms * 1e-3) / 1e12
         paths[p] = {"kernel": kernels[p], "ms": round(ms, 4), "ms_min": round(min(per_path[p]), 4),
                     "tflops": round(tf, 2), "peak_tflops": round(peaks[p], 1),
                     "frac_of_peak": round(tf / peaks[p], 4),
                     "frac_of_datasheet": round(tf / DATASHEET[p], 4)}
-    dominant = max(PATHS, key=lambda p: paths[p]["ms"])
+    dominant = max(paths_run, key=lambda p: paths[p]["ms"])
     dom = paths[dominant]
     kfile = "sgemm_simt.cu" if dominant == "f32_simt" else "umma_gemm.cu"
     roofline = {"kernel": dom["kernel"],
@@ -270,32 +279,36 @@ def run_ours(args):
                 "achieved": dom["tflops"], "peak": dom["peak_tflops"], "unit": "TFLOP/s",
                 "frac": dom["frac_of_peak"],
                 "peak_source": ("derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz"
-                                if dominant == "f32_simt" else peaks["source"] + " (MEASURED_PEAKS.json)"),
-                "traffic": _traffic_for(kfile, dom["kernel"])}
+                                if dominant == "f32_simt" else
+                                peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)" +
+                                (" x nominal tf32/bf16 ratio 1.1/2.25" if dominant == "tf32" else "")),
+                "traffic": _traffic_for(kfile, dom["kernel"], (Mx, Nx, Kx))}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(budget_s=args.cpu_budget)
 
     clocks = clk.summary()
+    default_run = tuple(paths_run) == PATHS and (Mx, Nx, Kx) == (M, N, K)
     line = {
         "metric": "GEMM TFLOPS (2MNK/s) per dtype at M=N=8192,K=4096; % of dense peak",
         "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32+tf32+f16(f32 acc)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32+tf32+f16(f32 acc)" if default_run
+        else "+".join(paths_run),
         "data": "synthetic (seeded uniform[-1,1) f32; N(0,1)/sqrt(K) f16)",
-        "config": {"workload": "gemm_f32_tf32_f16tn_8192x8192x4096", "M": M, "N": N, "K": K,
+        "config": {"workload": ("gemm_f32_tf32_f16tn_8192x8192x4096" if default_run else
+                                "gemm_%s_%dx%dx%d" % ("+".join(paths_run), Mx, Nx, Kx)),
+                   "M": Mx, "N": Nx, "K": Kx,
                    "alpha": 1.0, "beta": 0.0, "layout": "row-major NN (f32, tf32); TN (f16)",
-                   "step": "gemm_f32 + gemm_tf32 + gemm_f16_tn, one each",
+                   "step": " + ".join("one " + p for p in paths_run),
                    "l2": "flushed before every GEMM (512 MiB write, outside the timed events)",
                    "parallelism": "replicas x%d" % world},
         "paths": paths,
         "roofline": roofline,
         "clocks": clocks,
-        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "how": "pinned host A,B -> device copies, the C-ABI call, C -> pinned host; per path"},
-        "gpu_launches": 3 * args.steps,
+        "e2e": e2e,
+        "gpu_launches": len(paths_run) * args.steps,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -401,7 +414,18 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work per CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--paths", default=",".join(PATHS),
+                    help="comma-separated subset of %s (profiling runs)" % ",".join(PATHS))
+    ap.add_argument("--shape", default="%dx%dx%d" % (M, N, K), help="MxNxK (profiling runs)")
     args = ap.parse_args()
+    args.paths = [p for p in args.paths.split(",") if p]
+    if not args.paths or any(p not in PATHS for p in args.paths):
+        ap.error("--paths must name some of " + ",".join(PATHS))
+    args.paths = [p for p in PATHS if p in args.paths]
+    args.shape = tuple(int(v) for v in args.shape.lower().split("x"))
+    if len(args.shape) != 3 or min(args.shape) <= 0:
+        ap.error("--shape must be MxNxK")
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
