@@ -2,26 +2,27 @@
 //     C = alpha * A * B + beta * C, all row-major, FP32 fused multiply-add.
 //
 // Design (what is kept from the pages, and what changed for GB300):
-//   * Block tile 128 x 128, K slice 16, 256 threads, 8 x 8 outputs per thread
-//     held in registers -- the thread-tile idea of "SGEMM CUDA代码学习",
-//     "第 2 步" and of "CUDA GEMM：从基础写法到工程优化", "5. 2D Block Tiling".
-//   * A is staged transposed in shared memory (As[k][m]) and each thread's 8
-//     rows are split into two groups of 4 at m and m + 64, so every shared
+//   * Block tile 128 x 128, K slices of 16, 256 threads, 8 x 8 outputs per
+//     thread held in registers -- the thread-tile idea of "SGEMM CUDA代码学习",
+//     "第 2 步", and "CUDA GEMM：从基础写法到工程优化", "5. 2D Block Tiling".
+//   * A is staged transposed in shared memory (As[k][m]); each thread's 8 rows
+//     (and 8 columns) are two groups of 4 at m and m + 64, so every shared
 //     read is a conflict-free 16-byte load -- "SGEMM CUDA代码学习", "第 3 步".
-//     A 4-float pad on As rows, plus a warp-to-tile mapping in which each warp
-//     stores 16 rows x 2 k-quads, keeps the transposing stores conflict-free.
-//   * Threads are grouped so that a warp covers a 32 x 64 piece of the tile
-//     (warp tiling, "CUDA GEMM：从基础写法到工程优化", "10. Warp Tiling"):
-//     each 16-byte shared read then touches 64 or 128 distinct bytes, one
-//     shared-memory wavefront.
-//   * Double buffering through registers: the global loads of slice k+1 are
-//     issued before the FMAs of slice k and stored after them, one barrier
-//     per slice -- "SGEMM CUDA代码学习", "第 4 步".
-//   * Unlike the pages' kernels, every load is predicated: M, N and K tails
-//     read zeros and stores are masked, and no thread leaves before a
-//     barrier.  Operands whose pointers or leading dimensions are not 16-byte
-//     aligned take a scalar-load instantiation.
-//   * Epilogue: alpha * acc + beta * C_old, with C not read when beta == 0,
+//   * Warp tiling ("CUDA GEMM：从基础写法到工程优化", "10. Warp Tiling"): a warp
+//     covers a 32 x 64 piece of the tile, so each 16-byte shared read touches
+//     at most 128 distinct bytes (one wavefront).
+//   * A 4-stage ring of K slices filled with cp.async, the multi-stage
+//     asynchronous copy of "SGEMM CUDA代码学习", "第 5 步" and "CUDA GEMM：
+//     从基础写法到工程优化", "12. Async Copy Double Buffering".  A is copied
+//     element by element straight into its transposed place (no registers);
+//     B in 16-byte pieces.  Copies past M, N or K are zero-filled, so tails
+//     need no special loop, and no thread leaves before a barrier.
+//   * The FMAs are Blackwell's packed two-lane form (fma.rn.f32x2): each
+//     instruction updates two adjacent accumulators with two independent
+//     single-precision fused multiply-adds, halving the FMA issue slots.
+//     The arithmetic per output element is unchanged: one FP32 FMA per k, in
+//     k order.
+//   * Epilogue: alpha * acc + beta * C_old, C not read when beta == 0,
 //     16-byte stores where aligned.
 #include <cstdint>
 
@@ -35,91 +36,81 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int BK = 16;
+constexpr int STAGES = 4;
 constexpr int THREADS = 256;
 constexpr int AS_LD = BM + 4;  // padded row of the transposed A slice
 constexpr int kGroupM = 8;     // rasterisation group height, in tiles
 
-struct SimtSmem {
-    float As[2][BK][AS_LD];
-    float Bs[2][BK][BN];
+struct SimtStage {
+    float As[BK][AS_LD];
+    float Bs[BK][BN];
 };
+constexpr int SMEM_BYTES = STAGES * static_cast<int>(sizeof(SimtStage));
 
-// Global -> register staging of one K slice (2 float4 of A, 2 float4 of B per
-// thread).  Out-of-range elements read as zero.
-template <bool kVec>
-struct SliceRegs {
-    float4 a[2];
-    float4 b[2];
-};
-
-template <bool kVec>
-__device__ __forceinline__ void load_slice(SliceRegs<kVec> &r, const float *__restrict__ A,
-                                           int64_t lda, const float *__restrict__ B, int64_t ldb,
-                                           int64_t M, int64_t N, int64_t K, int64_t m0,
-                                           int64_t n0, int64_t k0, int warp, int lane, int tid)
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes)
 {
-    // A: thread covers row m = warp*16 + (lane & 15), k-quads 2i + (lane >> 4).
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int m = warp * 16 + (lane & 15);
-        const int kq = (i * 2 + (lane >> 4)) * 4;
-        const int64_t gm = m0 + m, gk = k0 + kq;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (gm < M) {
-            const float *p = A + gm * lda + gk;
-            if (kVec && gk + 3 < K) {
-                v = __ldg(reinterpret_cast<const float4 *>(p));
-            } else {
-                if (gk + 0 < K) v.x = __ldg(p + 0);
-                if (gk + 1 < K) v.y = __ldg(p + 1);
-                if (gk + 2 < K) v.z = __ldg(p + 2);
-                if (gk + 3 < K) v.w = __ldg(p + 3);
-            }
-        }
-        r.a[i] = v;
-    }
-    // B: a warp reads one full 128-float row of the slice.
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int idx = tid + i * THREADS;
-        const int k = idx >> 5;
-        const int nq = (idx & 31) * 4;
-        const int64_t gk = k0 + k, gn = n0 + nq;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (gk < K) {
-            const float *p = B + gk * ldb + gn;
-            if (kVec && gn + 3 < N) {
-                v = __ldg(reinterpret_cast<const float4 *>(p));
-            } else {
-                if (gn + 0 < N) v.x = __ldg(p + 0);
-                if (gn + 1 < N) v.y = __ldg(p + 1);
-                if (gn + 2 < N) v.z = __ldg(p + 2);
-                if (gn + 3 < N) v.w = __ldg(p + 3);
-            }
-        }
-        r.b[i] = v;
-    }
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
 }
 
-template <bool kVec>
-__device__ __forceinline__ void store_slice(const SliceRegs<kVec> &r, SimtSmem &s, int buf,
-                                            int warp, int lane, int tid)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
 {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+// Issue the copies of K slice `kt` into `stage`.
+//   A: element (m, k) of the slice, m = warp*4 + lane/8 + 32*(e%4),
+//      k = lane%8 + 8*(e/4), e = 0..7: a warp reads 8 consecutive k of 4 rows
+//      (one 32-byte sector each) and writes 32 distinct banks.
+//   B: row k = warp + 8*e, columns lane*4 .. lane*4+3, e = 0..1.
+template <bool kVec>
+__device__ __forceinline__ void load_slice(uint32_t stage_smem, const float *__restrict__ A,
+                                           int64_t lda, const float *__restrict__ B, int64_t ldb,
+                                           int64_t M, int64_t N, int64_t K, int64_t m0, int64_t n0,
+                                           int64_t kt, int warp, int lane)
+{
+    const int64_t k0 = kt * BK;
+    const uint32_t as = stage_smem;
+    const uint32_t bs = stage_smem + static_cast<uint32_t>(offsetof(SimtStage, Bs));
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int m = warp * 16 + (lane & 15);
-        const int kq = (i * 2 + (lane >> 4)) * 4;
-        s.As[buf][kq + 0][m] = r.a[i].x;
-        s.As[buf][kq + 1][m] = r.a[i].y;
-        s.As[buf][kq + 2][m] = r.a[i].z;
-        s.As[buf][kq + 3][m] = r.a[i].w;
+    for (int e = 0; e < 8; ++e) {
+        const int m = warp * 4 + (lane >> 3) + 32 * (e & 3);
+        const int k = (lane & 7) + 8 * (e >> 2);
+        const int64_t gm = m0 + m, gk = k0 + k;
+        const bool ok = gm < M && gk < K;
+        const float *src = ok ? A + gm * lda + gk : A;
+        cp_async4(as + static_cast<uint32_t>((k * AS_LD + m) * 4), src, ok ? 4u : 0u);
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int idx = tid + i * THREADS;
-        const int k = idx >> 5;
-        const int nq = (idx & 31) * 4;
-        *reinterpret_cast<float4 *>(&s.Bs[buf][k][nq]) = r.b[i];
+    for (int e = 0; e < 2; ++e) {
+        const int k = warp + 8 * e;
+        const int n = lane * 4;
+        const int64_t gk = k0 + k, gn = n0 + n;
+        const uint32_t dst = bs + static_cast<uint32_t>((k * BN + n) * 4);
+        if constexpr (kVec) {
+            const int64_t left = gk < K ? N - gn : 0;
+            const uint32_t bytes = left >= 4 ? 16u : (left > 0 ? static_cast<uint32_t>(left) * 4u : 0u);
+            cp_async16(dst, bytes ? B + gk * ldb + gn : B, bytes);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool ok = gk < K && gn + j < N;
+                cp_async4(dst + 4 * j, ok ? B + gk * ldb + gn + j : B, ok ? 4u : 0u);
+            }
+        }
     }
 }
 
@@ -161,7 +152,9 @@ __global__ void __launch_bounds__(THREADS, 2)
                       int64_t lda, const float *__restrict__ B, int64_t ldb, float beta,
                       float *__restrict__ C, int64_t ldc, bool vec_c)
 {
-    __shared__ __align__(16) SimtSmem s;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SimtStage *stages = reinterpret_cast<SimtStage *>(smem_raw);
+    const uint32_t smem0 = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -169,64 +162,85 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int ty = (warp >> 1) * 4 + (lane >> 3);  // 0..15
     const int tx = (warp & 1) * 8 + (lane & 7);    // 0..15
 
-    // Grouped rasterisation of a 1-D grid: runs of kGroupM consecutive
-    // blocks walk down M inside one N column, so blocks resident together
-    // share B columns and a short band of A rows in L2.
-    int64_t m_tile, n_tile;
+    // Grouped rasterisation of a 1-D grid: runs of kGroupM consecutive blocks
+    // walk down M inside one N column, so blocks resident together share B
+    // columns and a short band of A rows in L2.
+    int64_t m0, n0;
     {
         const int64_t tiles_m = (M + BM - 1) / BM;
         const int64_t b = blockIdx.x;
         const int64_t per_group = static_cast<int64_t>(kGroupM) * ((N + BN - 1) / BN);
         const int64_t g = b / per_group, r = b % per_group;
         const int64_t gm = tiles_m - g * kGroupM < kGroupM ? tiles_m - g * kGroupM : kGroupM;
-        m_tile = g * kGroupM + r % gm;
-        n_tile = r / gm;
+        m0 = (g * kGroupM + r % gm) * BM;
+        n0 = (r / gm) * BN;
     }
-    const int64_t m0 = m_tile * BM;
-    const int64_t n0 = n_tile * BN;
 
-    float acc[8][8];
+    float2 acc[8][4];  // acc[i][j]: row i, columns 2j and 2j+1 of the thread's 8
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
     const int64_t kt_count = (K + BK - 1) / BK;
-    SliceRegs<kVec> regs;
-    load_slice<kVec>(regs, A, lda, B, ldb, M, N, K, m0, n0, 0, warp, lane, tid);
-    store_slice<kVec>(regs, s, 0, warp, lane, tid);
-    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < kt_count)
+            load_slice<kVec>(smem0 + s * sizeof(SimtStage), A, lda, B, ldb, M, N, K, m0, n0, s, warp,
+                             lane);
+        cp_async_commit();
+    }
 
+    int read_stage = 0, write_stage = STAGES - 1;
     for (int64_t kt = 0; kt < kt_count; ++kt) {
-        const int buf = static_cast<int>(kt & 1);
-        const bool more = kt + 1 < kt_count;
-        if (more)
-            load_slice<kVec>(regs, A, lda, B, ldb, M, N, K, m0, n0, (kt + 1) * BK, warp, lane, tid);
-
+        cp_async_wait<STAGES - 2>();  // slice kt has landed (this thread's copies)
+        __syncthreads();              // ... everyone's; and slice kt-1 is consumed
+        if (kt + STAGES - 1 < kt_count)
+            load_slice<kVec>(smem0 + static_cast<uint32_t>(write_stage) * sizeof(SimtStage), A, lda,
+                             B, ldb, M, N, K, m0, n0, kt + STAGES - 1, warp, lane);
+        cp_async_commit();
+        write_stage = write_stage + 1 == STAGES ? 0 : write_stage + 1;
+        const SimtStage &st = stages[read_stage];
+        read_stage = read_stage + 1 == STAGES ? 0 : read_stage + 1;
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&s.As[buf][k][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&s.As[buf][k][ty * 4 + 64]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&s.Bs[buf][k][tx * 4]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&s.Bs[buf][k][tx * 4 + 64]);
+            const float4 a0 = *reinterpret_cast<const float4 *>(&st.As[k][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&st.As[k][ty * 4 + 64]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&st.Bs[k][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&st.Bs[k][tx * 4 + 64]);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                  make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
+                const float2 a2 = make_float2(av[i], av[i]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(a2, bp[j], acc[i][j]);
+            }
         }
-
-        if (more) store_slice<kVec>(regs, s, buf ^ 1, warp, lane, tid);
-        __syncthreads();
     }
+    cp_async_wait<0>();
 
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
-        epilogue_store(C, ldc, M, N, gm, n0 + tx * 4, &acc[i][0], alpha, beta, vec_c);
-        epilogue_store(C, ldc, M, N, gm, n0 + 64 + tx * 4, &acc[i][4], alpha, beta, vec_c);
+        const float lo[4] = {acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y};
+        const float hi[4] = {acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y};
+        epilogue_store(C, ldc, M, N, gm, n0 + tx * 4, lo, alpha, beta, vec_c);
+        epilogue_store(C, ldc, M, N, gm, n0 + 64 + tx * 4, hi, alpha, beta, vec_c);
     }
+}
+
+template <bool kVec>
+void launch_kernel(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                   const float *B, int64_t ldb, float beta, float *C, int64_t ldc, bool vec_c,
+                   cudaStream_t stream)
+{
+    cudaFuncSetAttribute(sgemm_simt_kernel<kVec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         SMEM_BYTES);
+    const int64_t blocks = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    sgemm_simt_kernel<kVec><<<static_cast<unsigned>(blocks), THREADS, SMEM_BYTES, stream>>>(
+        M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, vec_c);
 }
 
 }  // namespace
@@ -235,18 +249,15 @@ const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, cons
                               int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                               int64_t ldc, cudaStream_t stream)
 {
-    const bool vec_ab = aligned16(A) && aligned16(B) && (lda % 4 == 0) && (ldb % 4 == 0);
+    // 16-byte copies of B need a 16-byte aligned base and row pitch.
+    const bool vec_b = aligned16(B) && (ldb % 4 == 0);
     const bool vec_c = aligned16(C) && (ldc % 4 == 0);
-    const int64_t blocks = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const dim3 grid(static_cast<unsigned>(blocks));
-    if (vec_ab) {
-        sgemm_simt_kernel<true><<<grid, THREADS, 0, stream>>>(M, N, K, alpha, A, lda, B, ldb, beta,
-                                                              C, ldc, vec_c);
-        return "sgemm_simt_128x128x16_vec";
+    if (vec_b) {
+        launch_kernel<true>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, vec_c, stream);
+        return "sgemm_simt_128x128x16_ffma2_cpasync16";
     }
-    sgemm_simt_kernel<false><<<grid, THREADS, 0, stream>>>(M, N, K, alpha, A, lda, B, ldb, beta, C,
-                                                           ldc, vec_c);
-    return "sgemm_simt_128x128x16_scalar";
+    launch_kernel<false>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, vec_c, stream);
+    return "sgemm_simt_128x128x16_ffma2_cpasync4";
 }
 
 }  // namespace dgemm
