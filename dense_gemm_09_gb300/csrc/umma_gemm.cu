@@ -122,7 +122,8 @@ struct Params {
     int64_t lda, ldb;
 };
 
-__device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t &m0, int64_t &n0)
+__device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t &m0, int64_t &n0,
+                                            int64_t bm = BM)
 {
     // Groups of kGroupN tile columns; inside a group consecutive tiles share
     // one A row band and walk N, so the tiles in flight at once read a few
@@ -132,7 +133,7 @@ __device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t 
     const int64_t left = p.tiles_n - g * kGroupN;
     const int64_t gn = left < kGroupN ? left : kGroupN;
     n0 = (g * kGroupN + r % gn) * BN;
-    m0 = (r / gn) * BM;
+    m0 = (r / gn) * bm;
 }
 
 __device__ __forceinline__ void raise_abort(volatile int *abort_flag)
@@ -151,6 +152,25 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            raise_abort(abort_flag);
+            return false;
+        }
+    }
+}
+
+// Same, with cluster-scope acquire (barriers that the other CTA of a pair
+// arrives on, directly or through a multicast commit).
+__device__ __noinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort_flag)
+{
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
         if (*abort_flag) return false;
         if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
             raise_abort(abort_flag);
@@ -538,12 +558,249 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
         run_epilogue<kKind>(p, ctrl, tmem_base, warp, lane, abort_flag);
     }
 
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ CTA pairs
+//
+// The same GEMM on a pair of CTAs (a cluster of 2 on neighbouring SMs) that
+// share one tcgen05.mma of 256 x 256 x UMMA_K (cta_group::2): each CTA loads
+// its own 128 rows of A and one half (128 columns) of B, and holds its 128
+// rows of the 256 x 256 accumulator in its own TMEM.  Per CTA the operand
+// bytes per output tile fall from (128 + 256) to (128 + 128) rows per K slice,
+// which is what bounds the single-CTA kernel (L2 -> SM bandwidth).
+//   both CTAs  warp 0: TMA producer into the CTA's own 6-stage ring; both
+//              CTAs' loads complete on the even CTA's "full" barrier, which
+//              the even producer arms with the bytes of both halves;
+//              warps 2-5: epilogue of the CTA's 128 rows;
+//   even CTA   warp 1: the MMA issuer for the pair; it multicasts its commits
+//              to both CTAs' "empty" / "tmem_full" barriers.
+// The epilogue warps of both CTAs release an accumulator by arriving on the
+// even CTA's "tmem_empty" barrier (8 warp arrivals).
+
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_BM = 2 * BM;                    // rows per pair tile
+constexpr int PAIR_HALF_BYTES = 128 * ROW_BYTES;   // 16 KB: 128 rows of A or of B
+constexpr int PAIR_STAGE_BYTES = 2 * PAIR_HALF_BYTES;
+constexpr int PAIR_THREADS = 192;
+
+struct PairCtrl {
+    uint64_t full[PAIR_STAGES];   // even CTA: both halves of the stage landed
+    uint64_t empty[PAIR_STAGES];  // the pair's MMAs have read this stage
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + static_cast<int>(sizeof(PairCtrl));
+
+template <int kKind>
+constexpr uint32_t pair_idesc()
+{
+    return (Traits<kKind>::kIdesc & ~(0x1Fu << 24)) | (static_cast<uint32_t>(PAIR_BM >> 4) << 24);
+}
+
+template <int kKind>
+__device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
+                                              const Params &p, uint32_t smem_base, PairCtrl *ctrl,
+                                              uint32_t rank, volatile int *abort_flag)
+{
+    using T = Traits<kKind>;
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued = 0, issued_phase = 0;
+    bool ok = true;
+    for (int64_t t = cluster; ok && t < num_tiles; t += clusters) {
+        int64_t m0, n0;
+        tile_coords(t, p, m0, n0, PAIR_BM);
+        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint32_t full_local = ptx::smem_addr(&ctrl->full[stage]);
+            const uint32_t full = ptx::mapa(full_local, 0);  // the even CTA's barrier
+            if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, 2 * PAIR_STAGE_BYTES);
+            const uint32_t sa = smem_base + stage * PAIR_STAGE_BYTES;
+            const uint32_t sb = sa + PAIR_HALF_BYTES;
+            const int32_t kc = static_cast<int32_t>(kb * T::BK);
+            ptx::tma_load_2d_pair(sa, tmap_a, full, kc, static_cast<int32_t>(m0 + rank * 128));
+            const int64_t nb = n0 + rank * 128;  // this CTA's half of B
+            if constexpr (kKind == kF16) {
+                ptx::tma_load_2d_pair(sb, tmap_b, full, kc, static_cast<int32_t>(nb));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    ptx::tma_load_2d_pair(sb + c * 4096, tmap_b, full,
+                                          static_cast<int32_t>(nb + c * 32), kc);
+            }
+            issued |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == PAIR_STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok && rank == 0) {
+        // The even CTA's barrier counts both CTAs' bytes: wait (bounded) for
+        // the loads in flight before the pair leaves.
+        for (int s = 0; s < PAIR_STAGES; ++s)
+            if ((issued >> s) & 1u)
+                drain_wait(ptx::smem_addr(&ctrl->full[s]), (issued_phase >> s) & 1u);
+    }
+}
+
+template <int kKind>
+__device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, PairCtrl *ctrl,
+                                         uint32_t tmem_base, volatile int *abort_flag)
+{
+    using T = Traits<kKind>;
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int64_t t = cluster; ok && t < num_tiles; t += clusters) {
+        if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u,
+                                  abort_flag)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->full[stage]), phase, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sa = smem_base + stage * PAIR_STAGE_BYTES;
+            const uint32_t sb = sa + PAIR_HALF_BYTES;
+#pragma unroll
+            for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
+                const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
+                uint64_t db;
+                if constexpr (kKind == kF16)
+                    db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
+                else
+                    db = ptx::smem_desc(sb + k * 1024, 4096, 512, ptx::kSw128A32);
+                ptx::umma_pair<kKind>(d_tmem, da, db, pair_idesc<kKind>(), (kb | k) != 0 ? 1u : 0u);
+            }
+            ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), 0x3);
+            if (++stage == PAIR_STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->tmem_full[acc]), 0x3);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->mma_done), 0x1);
+    drain_wait(ptx::smem_addr(&ctrl->mma_done), 0);
+}
+
+template <int kKind>
+__device__ __forceinline__ void pair_epilogue(const Params &p, PairCtrl *ctrl, uint32_t tmem_base,
+                                              uint32_t rank, int warp, int lane,
+                                              volatile int *abort_flag)
+{
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const uint32_t quarter = static_cast<uint32_t>(warp & 3);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int64_t t = cluster; t < num_tiles; t += clusters) {
+        int64_t m0, n0;
+        tile_coords(t, p, m0, n0, PAIR_BM);
+        bool ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const int64_t row = m0 + rank * 128 + quarter * 32 + lane;
+        const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            __syncwarp();
+            ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+            ptx::tmem_ld_wait();
+            store_chunk<kKind>(p, row, n0 + c * 32, r);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_addr(&ctrl->tmem_empty[acc]), 0));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+}
+
+template <int kKind>
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
+    umma_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                     const __grid_constant__ CUtensorMap tmap_b, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    PairCtrl *ctrl = reinterpret_cast<PairCtrl *>(smem + PAIR_STAGES * PAIR_STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PAIR_STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&ctrl->full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_full[a]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_empty[a]), 8);
+        }
+        ptx::mbar_init(ptx::smem_addr(&ctrl->mma_done), 1);
+        ctrl->abort = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmap_a);
+        ptx::prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_addr(&ctrl->tmem_base), TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = ctrl->tmem_base;
+    volatile int *abort_flag = &ctrl->abort;
+    const uint32_t smem_base = ptx::smem_addr(smem);
+
+    if (warp == 0) {
+        if (lane == 0) pair_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) pair_mma<kKind>(p, smem_base, ctrl, tmem_base, abort_flag);
+    } else {
+        pair_epilogue<kKind>(p, ctrl, tmem_base, rank, warp, lane, abort_flag);
+    }
+
+    __syncwarp();  // the barrier below is warp-aligned: reconverge lane 0 with the rest
+    ptx::tc_fence_before();
+    ptx::cluster_sync();  // no CTA leaves while its partner may still signal it
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -595,6 +852,67 @@ bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, cudaS
     return true;
 }
 
+// Co-resident clusters of the pair kernel on the current device (0 if the
+// pair kernel cannot run), cached per device and operand kind.
+template <int kKind>
+int pair_clusters()
+{
+    constexpr int kMaxDevices = 64;
+    static int cached[kMaxDevices];
+    static std::once_flag once[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::call_once(once[dev], [dev] {
+        int n = 0;
+        if (cudaFuncSetAttribute(umma_pair_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PAIR_SMEM_BYTES) == cudaSuccess) {
+            int sms = 0;
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+            cfg.blockDim = dim3(PAIR_THREADS);
+            cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, umma_pair_kernel<kKind>, &cfg) != cudaSuccess) n = 0;
+        }
+        cudaGetLastError();  // a failed query leaves no sticky error behind
+        cached[dev] = n;
+    });
+    return cached[dev];
+}
+
+template <int kKind>
+bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, cudaStream_t stream)
+{
+    const int clusters = pair_clusters<kKind>();
+    if (clusters <= 0) return false;
+    const int64_t tiles = p.tiles_m * p.tiles_n;
+    const int64_t n = tiles < clusters ? tiles : clusters;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
+    cfg.blockDim = dim3(PAIR_THREADS);
+    cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind>, ma, mb, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
 Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
                    const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int bk, bool vec_c)
 {
@@ -628,6 +946,17 @@ const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, con
     // TMA needs 16-byte aligned bases and row pitches.
     const bool tma = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
     CUtensorMap ma{}, mb{};
+    if (tma && M > BM) {
+        // CTA pairs: B loaded in 128-row halves
+        Params pp = p;
+        pp.tiles_m = (M + PAIR_BM - 1) / PAIR_BM;
+        if (make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+            launch_pair<kF16>(ma, mb, pp, stream))
+            return "umma_f16_tn_pair_256x256x64_tma";
+    }
     if (tma && make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
         make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, BN,
@@ -645,6 +974,16 @@ const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const
                                  aligned16(C) && (ldc % 4 == 0));
     const bool tma = aligned16(A) && aligned16(B) && (lda * 4) % 16 == 0 && (ldb * 4) % 16 == 0;
     CUtensorMap ma{}, mb{};
+    if (tma && M > BM) {
+        Params pp = p;
+        pp.tiles_m = (M + PAIR_BM - 1) / PAIR_BM;
+        if (make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK,
+                     CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B) &&
+            launch_pair<kTF32>(ma, mb, pp, stream))
+            return "umma_tf32_pair_256x256x32_tma";
+    }
     if (tma && make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
         make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK,

@@ -237,4 +237,19 @@ def test_kernel_variant_names(path):
     want = {"f32": "sgemm_simt", "tf32": "umma_tf32", "f16_tn": "umma_f16_tn"}[path]
     assert dg.last_kernel().startswith(want)
     if path != "f32":
-        assert dg.last_kernel().endswith("_tma")
+        # M > 128 and 16-byte pitches: the CTA-pair kernel
+        assert dg.last_kernel().endswith("_tma") and "_pair_" in dg.last_kernel()
+        A, B, C = parity.host_operands(path, 128, 256, 256, seed=1)
+        got, _, _ = parity.run(path, A, B, C, 1.0, 0.0)
+        assert dg.last_kernel().endswith("_tma") and "_pair_" not in dg.last_kernel()
+        assert parity.worst_ratio(path, got, A, B, C, 1.0, 0.0) <= 1.0
+
+
+@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
+@pytest.mark.parametrize("M", [129, 200, 255, 256, 257, 383, 511, 640])
+def test_pair_kernel_m_tails(path, M):
+    # the pair tile is 256 rows: the odd CTA's rows run past M in these cases
+    N, K = 520, 264
+    A, B, C = parity.host_operands(path, M, N, K, seed=M)
+    got, _, _ = parity.run(path, A, B, C, 1.5, -0.25)
+    assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
