@@ -63,6 +63,8 @@ def lib():
         L.dgemm_status_string.restype = ctypes.c_char_p
         L.dgemm_device_status.argtypes = [ci]
         L.dgemm_device_status.restype = ci
+        L.dgemm_test_inject_stall.argtypes = [ctypes.c_uint64]
+        L.dgemm_test_inject_stall.restype = ci
         L.dgemm_last_kernel.argtypes = []
         L.dgemm_last_kernel.restype = ctypes.c_char_p
         _lib = L
@@ -76,6 +78,12 @@ def status_string(status: int) -> str:
 def device_status(clear: bool = True) -> int:
     """The kernels' device status word (synchronises the device)."""
     return lib().dgemm_device_status(1 if clear else 0)
+
+
+def test_inject_stall(wait_limit_ns: int) -> None:
+    """Test hook: the next tensor-core launch on this thread stalls on purpose
+    and its bounded waits (limit wait_limit_ns) run out; see include/dgemm.h."""
+    lib().dgemm_test_inject_stall(int(wait_limit_ns))
 
 
 def last_kernel() -> str:

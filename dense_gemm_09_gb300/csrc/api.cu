@@ -135,6 +135,12 @@ extern "C" int dgemm_device_status(int clear)
     return umma_read_status(clear);
 }
 
+extern "C" int dgemm_test_inject_stall(uint64_t wait_limit_ns)
+{
+    umma_inject_stall(wait_limit_ns);
+    return DGEMM_OK;
+}
+
 extern "C" const char *dgemm_last_kernel(void)
 {
     return t_last_kernel;

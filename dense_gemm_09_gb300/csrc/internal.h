@@ -45,4 +45,7 @@ const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const
 // Device status word of the tensor-core kernels (see dgemm_device_status).
 int umma_read_status(int clear);
 
+// Test hook behind dgemm_test_inject_stall.
+void umma_inject_stall(uint64_t wait_limit_ns);
+
 }  // namespace dgemm

@@ -67,7 +67,7 @@ constexpr int B_TILE_BYTES = BN * ROW_BYTES;       // 32 KB
 constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;                  // two f32 accumulators
 constexpr int kGroupN = 8;                         // tile-order group width
-constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s
+constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s, default wait bound
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
 
 enum { kF16 = 0, kTF32 = 1 };
@@ -97,14 +97,21 @@ struct Traits<kTF32> {
     static constexpr uint32_t kIdescKMajorB = kIdesc & ~(1u << 16);
 };
 
+// Per-CTA wait control: the abort flag every role polls and the wait limit.
+struct WaitCtl {
+    int abort;
+    int pad;
+    uint64_t limit_ns;
+};
+
 struct Ctrl {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
+    WaitCtl wait;
     uint32_t tmem_base;
-    int abort;
 };
 
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + static_cast<int>(sizeof(Ctrl));
@@ -120,6 +127,10 @@ struct Params {
     const void *A;
     const void *B;
     int64_t lda, ldb;
+    // bound of every mbarrier wait, and the test-only fault injection: when
+    // set, the producers never deliver the first stage, so the waits run out
+    uint64_t wait_limit_ns;
+    int inject_stall;
 };
 
 __device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t &m0, int64_t &n0,
@@ -136,25 +147,30 @@ __device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t 
     m0 = (r / gn) * bm;
 }
 
-__device__ __forceinline__ void raise_abort(volatile int *abort_flag)
+__device__ __forceinline__ bool aborted(const WaitCtl *wc)
+{
+    return *reinterpret_cast<const volatile int *>(&wc->abort) != 0;
+}
+
+__device__ __forceinline__ void raise_abort(WaitCtl *wc)
 {
     if (atomicExch(&g_umma_status, DGEMM_ERR_TIMEOUT) == 0) __threadfence();
-    *abort_flag = 1;
+    *reinterpret_cast<volatile int *>(&wc->abort) = 1;
 }
 
 // Bounded wait for the phase of the given parity; false on time-out or when
 // another role raised the abort flag.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, WaitCtl *wc)
 {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer_ns();
+    const uint64_t t0 = ptx::globaltimer_ns(), limit = wc->limit_ns;
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-            raise_abort(abort_flag);
+        if (aborted(wc)) return false;
+        if (ptx::globaltimer_ns() - t0 > limit) {
+            raise_abort(wc);
             return false;
         }
     }
@@ -162,18 +178,17 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
 
 // Same, with cluster-scope acquire (barriers that the other CTA of a pair
 // arrives on, directly or through a multicast commit).
-__device__ __noinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
-                                                  volatile int *abort_flag)
+__device__ __noinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, WaitCtl *wc)
 {
     if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer_ns();
+    const uint64_t t0 = ptx::globaltimer_ns(), limit = wc->limit_ns;
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-            raise_abort(abort_flag);
+        if (aborted(wc)) return false;
+        if (ptx::globaltimer_ns() - t0 > limit) {
+            raise_abort(wc);
             return false;
         }
     }
@@ -191,20 +206,29 @@ __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity)
 template <int kKind>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
                                              const Params &p, uint32_t smem_base, Ctrl *ctrl,
-                                             volatile int *abort_flag)
+                                             WaitCtl *wc)
 {
     using T = Traits<kKind>;
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     uint32_t stage = 0, phase = 0;
     uint32_t issued = 0, issued_phase = 0;  // per-stage: a load was issued / its phase
     bool ok = true;
+    bool stall = p.inject_stall != 0;  // test hook: never deliver the first stage
     for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0);
         for (int64_t kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, abort_flag)) {
+            if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
                 ok = false;
                 break;
+            }
+            if (stall) {
+                stall = false;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                continue;
             }
             const uint32_t full = ptx::smem_addr(&ctrl->full[stage]);
             ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
@@ -264,7 +288,7 @@ __device__ __forceinline__ void st_shared(uint32_t addr, E v)
 // stage's "full" barrier (128 arrivals).
 template <int kKind>
 __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_base, Ctrl *ctrl,
-                                                 int ptid, volatile int *abort_flag)
+                                                 int ptid, WaitCtl *wc)
 {
     using T = Traits<kKind>;
     using E = typename std::conditional<kKind == kF16, uint16_t, uint32_t>::type;
@@ -274,11 +298,20 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
     const E *__restrict__ B = static_cast<const E *>(p.B);
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     uint32_t stage = 0, phase = 0;
+    bool stall = p.inject_stall != 0;  // test hook: never deliver the first stage
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0);
         for (int64_t kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, abort_flag)) return;
+            if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) return;
+            if (stall) {
+                stall = false;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                continue;
+            }
             const int64_t k0 = kb * BK;
             const uint32_t sa = smem_base + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_TILE_BYTES;
@@ -331,21 +364,21 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
 
 template <int kKind, bool kTma>
 __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctrl *ctrl,
-                                        uint32_t tmem_base, volatile int *abort_flag)
+                                        uint32_t tmem_base, WaitCtl *wc)
 {
     using T = Traits<kKind>;
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        if (!wait_bounded(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u, abort_flag)) {
+        if (!wait_bounded(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u, wc)) {
             ok = false;
             break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int64_t kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bounded(ptx::smem_addr(&ctrl->full[stage]), phase, abort_flag)) {
+            if (!wait_bounded(ptx::smem_addr(&ctrl->full[stage]), phase, wc)) {
                 ok = false;
                 break;
             }
@@ -465,7 +498,7 @@ __device__ __forceinline__ void store_chunk(const Params &p, int64_t row, int64_
 
 template <int kKind>
 __device__ __forceinline__ void run_epilogue(const Params &p, Ctrl *ctrl, uint32_t tmem_base,
-                                             int warp, int lane, volatile int *abort_flag)
+                                             int warp, int lane, WaitCtl *wc)
 {
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const uint32_t quarter = static_cast<uint32_t>(warp & 3);  // TMEM lanes this warp may read
@@ -473,7 +506,7 @@ __device__ __forceinline__ void run_epilogue(const Params &p, Ctrl *ctrl, uint32
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0);
-        bool ok = wait_bounded(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, abort_flag);
+        bool ok = wait_bounded(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, wc);
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
         if (!ok) break;
         ptx::tc_fence_after();
@@ -528,7 +561,8 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
             ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_empty[a]), 4 * 32);
         }
         ptx::mbar_init(ptx::smem_addr(&ctrl->mma_done), 1);
-        ctrl->abort = 0;
+        ctrl->wait.abort = 0;
+        ctrl->wait.limit_ns = p.wait_limit_ns;
         ptx::fence_mbarrier_init();
     }
     if (kTma && warp == 0 && lane == 0) {
@@ -543,19 +577,19 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = ctrl->tmem_base;
-    volatile int *abort_flag = &ctrl->abort;
+    WaitCtl *wc = &ctrl->wait;
     const uint32_t smem_base = ptx::smem_addr(smem);
 
     if (warp < kMmaWarp) {
         if constexpr (kTma) {
-            if (lane == 0) run_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, abort_flag);
+            if (lane == 0) run_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, wc);
         } else {
-            run_reg_producer<kKind>(p, smem_base, ctrl, threadIdx.x, abort_flag);
+            run_reg_producer<kKind>(p, smem_base, ctrl, threadIdx.x, wc);
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) run_mma<kKind, kTma>(p, smem_base, ctrl, tmem_base, abort_flag);
+        if (lane == 0) run_mma<kKind, kTma>(p, smem_base, ctrl, tmem_base, wc);
     } else {
-        run_epilogue<kKind>(p, ctrl, tmem_base, warp, lane, abort_flag);
+        run_epilogue<kKind>(p, ctrl, tmem_base, warp, lane, wc);
     }
 
     __syncwarp();
@@ -597,8 +631,8 @@ struct PairCtrl {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
+    WaitCtl wait;
     uint32_t tmem_base;
-    int abort;
 };
 
 constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + static_cast<int>(sizeof(PairCtrl));
@@ -612,7 +646,7 @@ constexpr uint32_t pair_idesc()
 template <int kKind>
 __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
                                               const Params &p, uint32_t smem_base, PairCtrl *ctrl,
-                                              uint32_t rank, volatile int *abort_flag)
+                                              uint32_t rank, WaitCtl *wc)
 {
     using T = Traits<kKind>;
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
@@ -620,13 +654,22 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
     uint32_t stage = 0, phase = 0;
     uint32_t issued = 0, issued_phase = 0;
     bool ok = true;
+    bool stall = p.inject_stall != 0;  // test hook: never deliver the first stage
     for (int64_t t = cluster; ok && t < num_tiles; t += clusters) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0, PAIR_BM);
         for (int64_t kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, abort_flag)) {
+            if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
                 ok = false;
                 break;
+            }
+            if (stall) {
+                stall = false;
+                if (++stage == PAIR_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                continue;
             }
             const uint32_t full_local = ptx::smem_addr(&ctrl->full[stage]);
             const uint32_t full = ptx::mapa(full_local, 0);  // the even CTA's barrier
@@ -663,7 +706,7 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
 
 template <int kKind>
 __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, PairCtrl *ctrl,
-                                         uint32_t tmem_base, volatile int *abort_flag)
+                                         uint32_t tmem_base, WaitCtl *wc)
 {
     using T = Traits<kKind>;
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
@@ -672,14 +715,14 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
     bool ok = true;
     for (int64_t t = cluster; ok && t < num_tiles; t += clusters) {
         if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u,
-                                  abort_flag)) {
+                                  wc)) {
             ok = false;
             break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int64_t kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->full[stage]), phase, abort_flag)) {
+            if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->full[stage]), phase, wc)) {
                 ok = false;
                 break;
             }
@@ -714,7 +757,7 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
 template <int kKind>
 __device__ __forceinline__ void pair_epilogue(const Params &p, PairCtrl *ctrl, uint32_t tmem_base,
                                               uint32_t rank, int warp, int lane,
-                                              volatile int *abort_flag)
+                                              WaitCtl *wc)
 {
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
@@ -723,7 +766,7 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, PairCtrl *ctrl, u
     for (int64_t t = cluster; t < num_tiles; t += clusters) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0, PAIR_BM);
-        bool ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, abort_flag);
+        bool ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
@@ -768,7 +811,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_empty[a]), 8);
         }
         ptx::mbar_init(ptx::smem_addr(&ctrl->mma_done), 1);
-        ctrl->abort = 0;
+        ctrl->wait.abort = 0;
+        ctrl->wait.limit_ns = p.wait_limit_ns;
         ptx::fence_mbarrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -783,15 +827,15 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     ptx::tc_fence_after();
     const uint32_t tmem_base = ctrl->tmem_base;
-    volatile int *abort_flag = &ctrl->abort;
+    WaitCtl *wc = &ctrl->wait;
     const uint32_t smem_base = ptx::smem_addr(smem);
 
     if (warp == 0) {
-        if (lane == 0) pair_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, abort_flag);
+        if (lane == 0) pair_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) pair_mma<kKind>(p, smem_base, ctrl, tmem_base, abort_flag);
+        if (lane == 0 && rank == 0) pair_mma<kKind>(p, smem_base, ctrl, tmem_base, wc);
     } else {
-        pair_epilogue<kKind>(p, ctrl, tmem_base, rank, warp, lane, abort_flag);
+        pair_epilogue<kKind>(p, ctrl, tmem_base, rank, warp, lane, wc);
     }
 
     __syncwarp();  // the barrier below is warp-aligned: reconverge lane 0 with the rest
@@ -913,10 +957,17 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, 
     return true;
 }
 
+// One-shot test hook (dgemm_test_inject_stall): applies to the next
+// tensor-core launch made by this host thread.
+thread_local uint64_t t_inject_limit_ns = 0;
+
 Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
                    const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int bk, bool vec_c)
 {
     Params p;
+    p.inject_stall = t_inject_limit_ns ? 1 : 0;
+    p.wait_limit_ns = t_inject_limit_ns ? t_inject_limit_ns : kWaitLimitNs;
+    t_inject_limit_ns = 0;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -991,6 +1042,11 @@ const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const
         return launch<kTF32, true>(ma, mb, p, stream, dev) ? "umma_tf32_128x256x32_tma" : nullptr;
     }
     return launch<kTF32, false>(ma, mb, p, stream, dev) ? "umma_tf32_128x256x32_ldst" : nullptr;
+}
+
+void umma_inject_stall(uint64_t wait_limit_ns)
+{
+    t_inject_limit_ns = wait_limit_ns ? wait_limit_ns : 1;
 }
 
 int umma_read_status(int clear)
