@@ -213,6 +213,32 @@ __device__ __forceinline__ uint32_t mapa(uint32_t smem, uint32_t rank)
     return r;
 }
 
+// Load from the shared memory of a cluster CTA (a shared::cluster address).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// Store to the shared memory of a cluster CTA (a shared::cluster address).
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t cluster_addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // Arrive on an mbarrier of another CTA of the cluster (cluster-scope release).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {

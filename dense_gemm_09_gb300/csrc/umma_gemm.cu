@@ -131,6 +131,9 @@ struct Params {
     // set, the producers never deliver the first stage, so the waits run out
     uint64_t wait_limit_ns;
     int inject_stall;
+    // split-K: the S CTAs of a cluster share one output tile, each summing a
+    // contiguous range of K blocks (1 = no split)
+    int splitk;
 };
 
 __device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t &m0, int64_t &n0,
@@ -145,6 +148,32 @@ __device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t 
     const int64_t gn = left < kGroupN ? left : kGroupN;
     n0 = (g * kGroupN + r % gn) * BN;
     m0 = (r / gn) * bm;
+}
+
+// The work of one CTA: tiles t0, t0 + dt, ... and, with split-K, the K
+// blocks [kb0, kb1) of each (the S CTAs of a cluster share a tile; rank r
+// takes the r-th of S near-equal contiguous ranges).
+struct Sched {
+    int64_t t0, dt, kb0, kb1;
+};
+
+__device__ __forceinline__ Sched schedule(const Params &p)
+{
+    Sched s;
+    const int S = p.splitk;
+    if (S > 1) {
+        const int64_t r = ptx::cluster_ctarank();
+        s.t0 = blockIdx.x / S;
+        s.dt = gridDim.x / S;
+        s.kb0 = r * p.num_kb / S;
+        s.kb1 = (r + 1) * p.num_kb / S;
+    } else {
+        s.t0 = blockIdx.x;
+        s.dt = gridDim.x;
+        s.kb0 = 0;
+        s.kb1 = p.num_kb;
+    }
+    return s;
 }
 
 __device__ __forceinline__ bool aborted(const WaitCtl *wc)
@@ -210,14 +239,15 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
 {
     using T = Traits<kKind>;
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const Sched sc = schedule(p);
     uint32_t stage = 0, phase = 0;
     uint32_t issued = 0, issued_phase = 0;  // per-stage: a load was issued / its phase
     bool ok = true;
     bool stall = p.inject_stall != 0;  // test hook: never deliver the first stage
-    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+    for (int64_t t = sc.t0; ok && t < num_tiles; t += sc.dt) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0);
-        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+        for (int64_t kb = sc.kb0; kb < sc.kb1; ++kb) {
             if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
                 ok = false;
                 break;
@@ -297,12 +327,13 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
     const E *__restrict__ A = static_cast<const E *>(p.A);
     const E *__restrict__ B = static_cast<const E *>(p.B);
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const Sched sc = schedule(p);
     uint32_t stage = 0, phase = 0;
     bool stall = p.inject_stall != 0;  // test hook: never deliver the first stage
-    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int64_t t = sc.t0; t < num_tiles; t += sc.dt) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0);
-        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+        for (int64_t kb = sc.kb0; kb < sc.kb1; ++kb) {
             if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) return;
             if (stall) {
                 stall = false;
@@ -368,16 +399,17 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
 {
     using T = Traits<kKind>;
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const Sched sc = schedule(p);
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+    for (int64_t t = sc.t0; ok && t < num_tiles; t += sc.dt) {
         if (!wait_bounded(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u, wc)) {
             ok = false;
             break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+        for (int64_t kb = sc.kb0; kb < sc.kb1; ++kb) {
             if (!wait_bounded(ptx::smem_addr(&ctrl->full[stage]), phase, wc)) {
                 ok = false;
                 break;
@@ -401,7 +433,7 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
                     db = ptx::smem_desc(sb + k * 1024, 4096, 512, ptx::kSw128A32);
                 }
                 ptx::umma<kKind>(d_tmem, da, db, kTma ? T::kIdesc : T::kIdescKMajorB,
-                                 (kb | k) != 0 ? 1u : 0u);
+                                 (kb != sc.kb0 || k != 0) ? 1u : 0u);
             }
             ptx::umma_commit(ptx::smem_addr(&ctrl->empty[stage]));
             if (++stage == STAGES) {
@@ -501,9 +533,10 @@ __device__ __forceinline__ void run_epilogue(const Params &p, Ctrl *ctrl, uint32
                                              int warp, int lane, WaitCtl *wc)
 {
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const Sched sc = schedule(p);
     const uint32_t quarter = static_cast<uint32_t>(warp & 3);  // TMEM lanes this warp may read
     uint32_t acc = 0, acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int64_t t = sc.t0; t < num_tiles; t += sc.dt) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0);
         bool ok = wait_bounded(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, wc);
@@ -524,6 +557,98 @@ __device__ __forceinline__ void run_epilogue(const Params &p, Ctrl *ctrl, uint32
         ptx::mbar_arrive(ptx::smem_addr(&ctrl->tmem_empty[acc]));
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
+    }
+}
+
+// ---- split-K: the partial sums of a tile meet in distributed shared memory
+//
+// Each of the S CTAs of a cluster has summed its K range of the same tile in
+// TMEM.  The tile's eight 32-column chunks are owned round-robin: chunk c by
+// rank c mod S.  "push": every CTA copies the chunks it does not own from
+// TMEM straight into the owner's (now idle) stage buffers -- remote stores,
+// which the thread does not wait for.  After a cluster barrier, "reduce":
+// the owner adds, for each row and column, the S partials in rank order
+// 0..S-1 (its own taken from TMEM, the others from its shared memory), so the
+// sum does not depend on timing, and stores alpha * sum + beta * C_old.
+// Layout of the receive buffers: [slot = sender among the other S-1
+// ranks][owned chunk][column j][row], 4-byte words; consecutive threads
+// (rows) touch consecutive words.
+
+__device__ __forceinline__ uint32_t recv_offset(uint32_t slot, uint32_t chunk_idx, uint32_t S,
+                                                int j, int row)
+{
+    const uint32_t owned_max = (BN / 32 + S - 1) / S;
+    return (((slot * owned_max + chunk_idx) * 32u + static_cast<uint32_t>(j)) * BM +
+            static_cast<uint32_t>(row)) * 4u;
+}
+
+__device__ __forceinline__ void splitk_push(const Params &p, Ctrl *ctrl, uint32_t tmem_base,
+                                            uint32_t smem_base, int warp, int lane, WaitCtl *wc)
+{
+    const uint32_t quarter = static_cast<uint32_t>(warp & 3);
+    bool ok = wait_bounded(ptx::smem_addr(&ctrl->tmem_full[0]), 0, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return;
+    ptx::tc_fence_after();
+    const uint32_t S = static_cast<uint32_t>(p.splitk);
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int row = static_cast<int>(quarter * 32 + lane);
+    const uint32_t taddr = tmem_base + ((quarter * 32u) << 16);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        const uint32_t owner = static_cast<uint32_t>(c) % S;
+        if (owner == rank) continue;
+        uint32_t r[32];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+        ptx::tmem_ld_wait();
+        const uint32_t slot = rank < owner ? rank : rank - 1;
+        const uint32_t base = ptx::mapa(smem_base + recv_offset(slot, static_cast<uint32_t>(c) / S, S, 0, row),
+                                        owner);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            ptx::st_shared_cluster_f32(base + static_cast<uint32_t>(j) * BM * 4u, __uint_as_float(r[j]));
+    }
+}
+
+template <int kKind>
+__device__ __forceinline__ void splitk_reduce(const Params &p, uint32_t tmem_base,
+                                              uint32_t smem_base, int warp, int lane, WaitCtl *wc)
+{
+    if (__any_sync(0xffffffffu, aborted(wc))) return;
+    const uint32_t quarter = static_cast<uint32_t>(warp & 3);
+    const uint32_t S = static_cast<uint32_t>(p.splitk);
+    const uint32_t rank = ptx::cluster_ctarank();
+    int64_t m0, n0;
+    tile_coords(blockIdx.x / S, p, m0, n0);
+    const int row = static_cast<int>(quarter * 32 + lane);
+    const uint32_t taddr = tmem_base + ((quarter * 32u) << 16);
+    ptx::tc_fence_after();
+#pragma unroll 1
+    for (uint32_t c = rank; c < BN / 32; c += S) {
+        uint32_t own[32];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(taddr + c * 32, own);
+        ptx::tmem_ld_wait();
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+        for (uint32_t q = 0; q < S; ++q) {
+            if (q == rank) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[j] += __uint_as_float(own[j]);
+            } else {
+                const uint32_t slot = q < rank ? q : q - 1;
+                const uint32_t base = smem_base + recv_offset(slot, c / S, S, 0, row);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    acc[j] += ptx::ld_shared_f32(base + static_cast<uint32_t>(j) * BM * 4u);
+            }
+        }
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
+        store_chunk<kKind>(p, m0 + row, n0 + c * 32, r);
     }
 }
 
@@ -589,7 +714,19 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
     } else if (warp == kMmaWarp) {
         if (lane == 0) run_mma<kKind, kTma>(p, smem_base, ctrl, tmem_base, wc);
     } else {
-        run_epilogue<kKind>(p, ctrl, tmem_base, warp, lane, wc);
+        if (p.splitk > 1)
+            splitk_push(p, ctrl, tmem_base, smem_base, warp, lane, wc);
+        else
+            run_epilogue<kKind>(p, ctrl, tmem_base, warp, lane, wc);
+    }
+
+    if (p.splitk > 1) {  // uniform over the cluster
+        __syncwarp();
+        ptx::tc_fence_before();
+        ptx::cluster_sync();  // every pushed partial has landed in its owner
+        if (warp > kMmaWarp) splitk_reduce<kKind>(p, tmem_base, smem_base, warp, lane, wc);
+        __syncwarp();
+        ptx::cluster_sync();  // keep the cluster together until every owner is done
     }
 
     __syncwarp();
@@ -966,6 +1103,7 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, 
 {
     Params p;
     p.inject_stall = t_inject_limit_ns ? 1 : 0;
+    p.splitk = 1;
     p.wait_limit_ns = t_inject_limit_ns ? t_inject_limit_ns : kWaitLimitNs;
     t_inject_limit_ns = 0;
     p.M = M;
@@ -986,6 +1124,127 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, 
     return p;
 }
 
+// Clusters of `size` CTAs of the single-CTA kernel that can be resident at
+// once on the current device (0 if none), cached per device, kind and size.
+template <int kKind>
+int cluster_capacity(int size)
+{
+    constexpr int kMaxDevices = 64;
+    static int cached[kMaxDevices][9];
+    static std::once_flag once[kMaxDevices];
+    int dev = 0;
+    if (size < 2 || size > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return 0;
+    std::call_once(once[dev], [dev] {
+        for (int s = 0; s < 9; ++s) cached[dev][s] = 0;
+        if (cudaFuncSetAttribute(umma_gemm_kernel<kKind, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        for (int s = 2; s <= 8; ++s) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(s);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % s));
+            cfg.blockDim = dim3(cta_threads<true>());
+            cfg.dynamicSmemBytes = SMEM_BYTES;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, umma_gemm_kernel<kKind, true>, &cfg) != cudaSuccess)
+                n = 0;
+            cached[dev][s] = n;
+        }
+        cudaGetLastError();
+    });
+    return cached[dev][size];
+}
+
+// Split factor for problems with few output tiles: the largest S <= 8 (the
+// portable cluster size) such that every range has at least 8 K blocks and
+// all tiles x S CTAs are resident in one wave of clusters.  1 = no split.
+template <int kKind>
+int choose_splitk(const Params &p, int sm_count)
+{
+    const int64_t tiles = p.tiles_m * p.tiles_n;  // single-CTA 128 x 256 tiles
+    if (tiles * 2 > sm_count) return 1;
+    int64_t s = sm_count / tiles;
+    if (s > p.num_kb / 8) s = p.num_kb / 8;
+    if (s > 8) s = 8;
+    for (; s >= 2; --s)
+        if (tiles <= cluster_capacity<kKind>(static_cast<int>(s))) return static_cast<int>(s);
+    return 1;
+}
+
+template <int kKind>
+bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p,
+                   cudaStream_t stream)
+{
+    if (cudaFuncSetAttribute(umma_gemm_kernel<kKind, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splitk);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(p.tiles_m * p.tiles_n * p.splitk));
+    cfg.blockDim = dim3(cta_threads<true>());
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, umma_gemm_kernel<kKind, true>, ma, mb, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
+const char *splitk_name(int kind, int s)
+{
+    static const char *f16[9] = {"", "", "umma_f16_tn_splitk2_128x256x64_tma",
+                                 "umma_f16_tn_splitk3_128x256x64_tma", "umma_f16_tn_splitk4_128x256x64_tma",
+                                 "umma_f16_tn_splitk5_128x256x64_tma", "umma_f16_tn_splitk6_128x256x64_tma",
+                                 "umma_f16_tn_splitk7_128x256x64_tma", "umma_f16_tn_splitk8_128x256x64_tma"};
+    static const char *tf32[9] = {"", "", "umma_tf32_splitk2_128x256x32_tma",
+                                  "umma_tf32_splitk3_128x256x32_tma", "umma_tf32_splitk4_128x256x32_tma",
+                                  "umma_tf32_splitk5_128x256x32_tma", "umma_tf32_splitk6_128x256x32_tma",
+                                  "umma_tf32_splitk7_128x256x32_tma", "umma_tf32_splitk8_128x256x32_tma"};
+    return kind == kF16 ? f16[s] : tf32[s];
+}
+
+// TMA-capable operands: split-K for few tiles, CTA pairs for M > 128, else
+// the persistent single-CTA kernel.  ma / mb: maps with the single-CTA boxes;
+// mb_pair: B with 128-row boxes.
+template <int kKind>
+const char *dispatch_tma(const Params &p, const CUtensorMap &ma, const CUtensorMap &mb,
+                         const CUtensorMap *mb_pair, cudaStream_t stream, const DeviceInfo &dev,
+                         const char *pair_name, const char *single_name)
+{
+    const int S = choose_splitk<kKind>(p, dev.sm_count);
+    if (S > 1) {
+        Params ps = p;
+        ps.splitk = S;
+        if (launch_splitk<kKind>(ma, mb, ps, stream)) return splitk_name(kKind, S);
+    }
+    if (mb_pair && p.M > BM) {
+        Params pp = p;
+        pp.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
+        if (launch_pair<kKind>(ma, *mb_pair, pp, stream)) return pair_name;
+    }
+    return launch<kKind, true>(ma, mb, p, stream, dev) ? single_name : nullptr;
+}
+
 }  // namespace
 
 const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
@@ -996,23 +1255,16 @@ const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, con
                                  aligned16(C) && (ldc % 8 == 0));
     // TMA needs 16-byte aligned bases and row pitches.
     const bool tma = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
-    CUtensorMap ma{}, mb{};
-    if (tma && M > BM) {
-        // CTA pairs: B loaded in 128-row halves
-        Params pp = p;
-        pp.tiles_m = (M + PAIR_BM - 1) / PAIR_BM;
-        if (make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM,
-                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, 128,
-                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-            launch_pair<kF16>(ma, mb, pp, stream))
-            return "umma_f16_tn_pair_256x256x64_tma";
-    }
-    if (tma && make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM,
-                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+    CUtensorMap ma{}, mb{}, mbp{};
+    if (tma &&
+        make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) &&
         make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, BN,
                  CU_TENSOR_MAP_SWIZZLE_128B)) {
-        return launch<kF16, true>(ma, mb, p, stream, dev) ? "umma_f16_tn_128x256x64_tma" : nullptr;
+        const bool pair_map = make_map(&mbp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2,
+                                       Traits<kF16>::BK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        return dispatch_tma<kF16>(p, ma, mb, pair_map ? &mbp : nullptr, stream, dev,
+                                  "umma_f16_tn_pair_256x256x64_tma", "umma_f16_tn_128x256x64_tma");
     }
     return launch<kF16, false>(ma, mb, p, stream, dev) ? "umma_f16_tn_128x256x64_ldst" : nullptr;
 }
@@ -1025,21 +1277,14 @@ const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const
                                  aligned16(C) && (ldc % 4 == 0));
     const bool tma = aligned16(A) && aligned16(B) && (lda * 4) % 16 == 0 && (ldb * 4) % 16 == 0;
     CUtensorMap ma{}, mb{};
-    if (tma && M > BM) {
-        Params pp = p;
-        pp.tiles_m = (M + PAIR_BM - 1) / PAIR_BM;
-        if (make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM,
-                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK,
-                     CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B) &&
-            launch_pair<kTF32>(ma, mb, pp, stream))
-            return "umma_tf32_pair_256x256x32_tma";
-    }
-    if (tma && make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM,
-                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+    if (tma &&
+        make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) &&
         make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK,
                  CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)) {
-        return launch<kTF32, true>(ma, mb, p, stream, dev) ? "umma_tf32_128x256x32_tma" : nullptr;
+        // TF32's B boxes are 32 x 32 for both kernels: one map serves both
+        return dispatch_tma<kTF32>(p, ma, mb, &mb, stream, dev, "umma_tf32_pair_256x256x32_tma",
+                                   "umma_tf32_128x256x32_tma");
     }
     return launch<kTF32, false>(ma, mb, p, stream, dev) ? "umma_tf32_128x256x32_ldst" : nullptr;
 }

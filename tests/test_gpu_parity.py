@@ -253,3 +253,45 @@ def test_pair_kernel_m_tails(path, M):
     A, B, C = parity.host_operands(path, M, N, K, seed=M)
     got, _, _ = parity.run(path, A, B, C, 1.5, -0.25)
     assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+# Few output tiles and a long K: the split-K kernel (a cluster of S CTAs per
+# tile, partials reduced in distributed shared memory).
+SPLITK_CASES = [
+    ("f16_tn", (100, 1000, 2048)),   # 4 tiles, S = 8
+    ("f16_tn", (64, 512, 1024)),     # 2 tiles, S = 4
+    ("f16_tn", (300, 512, 4096)),    # M > 128 still splits when tiles are few
+    ("f16_tn", (127, 2048, 1000)),   # K tail inside the last range
+    ("tf32", (100, 520, 1000)),      # K tail, S = 8
+    ("tf32", (256, 256, 2048)),
+]
+
+
+@pytest.mark.parametrize("path,shape", SPLITK_CASES)
+def test_splitk_kernel(path, shape):
+    import dense_gemm_09_gb300 as dg
+    M, N, K = shape
+    A, B, C = parity.host_operands(path, M, N, K, seed=M * 3 + N)
+    got, _, _ = parity.run(path, A, B, C, 1.5, -0.25)
+    assert "_splitk" in dg.last_kernel(), dg.last_kernel()
+    assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
+def test_splitk_integers_bit_exact(path):
+    import dense_gemm_09_gb300 as dg
+    M, N, K = 120, 600, 2048
+    A, B, C = parity.host_operands(path, M, N, K, seed=31, dist="int")
+    got, _, _ = parity.run(path, A, B, C, 1.0, 1.0)
+    assert "_splitk" in dg.last_kernel()
+    ref, _ = parity.reference(path, A, B, C, 1.0, 1.0)
+    assert np.array_equal(got.numpy().astype(np.float64), ref)
+
+
+def test_splitk_is_deterministic():
+    # the partials are added in rank order, whatever the timing
+    import dense_gemm_09_gb300 as dg
+    A, B, C = parity.host_operands("f16_tn", 127, 1024, 4096, seed=5)
+    outs = [parity.run("f16_tn", A, B, C, 1.0, 0.0)[0] for _ in range(3)]
+    assert "_splitk" in dg.last_kernel()
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
