@@ -110,11 +110,12 @@ struct Ctrl {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
+    uint64_t never;  // test hook: a barrier nothing arrives at
     WaitCtl wait;
     uint32_t tmem_base;
 };
 
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + static_cast<int>(sizeof(Ctrl));
+
 
 struct Params {
     int64_t M, N, K;
@@ -128,12 +129,16 @@ struct Params {
     const void *B;
     int64_t lda, ldb;
     // bound of every mbarrier wait, and the test-only fault injection: when
-    // set, the producers never deliver the first stage, so the waits run out
+    // set, the MMA issuer first waits on a barrier nothing arrives at, so the
+    // waits run out
     uint64_t wait_limit_ns;
     int inject_stall;
     // split-K: the S CTAs of a cluster share one output tile, each summing a
     // contiguous range of K blocks (1 = no split)
     int splitk;
+    // epilogue stores C through shared-memory boxes and TMA (else direct
+    // 16-byte / scalar stores)
+    int tma_store;
 };
 
 __device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t &m0, int64_t &n0,
@@ -243,7 +248,6 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
     uint32_t stage = 0, phase = 0;
     uint32_t issued = 0, issued_phase = 0;  // per-stage: a load was issued / its phase
     bool ok = true;
-    bool stall = p.inject_stall != 0;  // test hook: never deliver the first stage
     for (int64_t t = sc.t0; ok && t < num_tiles; t += sc.dt) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0);
@@ -251,14 +255,6 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
             if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
                 ok = false;
                 break;
-            }
-            if (stall) {
-                stall = false;
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                continue;
             }
             const uint32_t full = ptx::smem_addr(&ctrl->full[stage]);
             ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
@@ -329,20 +325,11 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const Sched sc = schedule(p);
     uint32_t stage = 0, phase = 0;
-    bool stall = p.inject_stall != 0;  // test hook: never deliver the first stage
     for (int64_t t = sc.t0; t < num_tiles; t += sc.dt) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0);
         for (int64_t kb = sc.kb0; kb < sc.kb1; ++kb) {
             if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) return;
-            if (stall) {
-                stall = false;
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                continue;
-            }
             const int64_t k0 = kb * BK;
             const uint32_t sa = smem_base + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_TILE_BYTES;
@@ -401,7 +388,8 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const Sched sc = schedule(p);
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-    bool ok = true;
+    // test hook: wait on a barrier nothing arrives at, so the wait runs out
+    bool ok = !p.inject_stall || wait_bounded(ptx::smem_addr(&ctrl->never), 0, wc);
     for (int64_t t = sc.t0; ok && t < num_tiles; t += sc.dt) {
         if (!wait_bounded(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u, wc)) {
             ok = false;
@@ -528,23 +516,82 @@ __device__ __forceinline__ void store_chunk(const Params &p, int64_t row, int64_
     }
 }
 
+// ---- epilogue through shared memory and TMA stores
+//
+// Each epilogue warp owns two 4 KB staging boxes of 32 rows x 128 bytes (64
+// f16 or 32 f32 columns), written with the 128-byte swizzle (16-byte chunk j
+// of row r at chunk position j ^ (r mod 8): the 8 rows a wavefront touches
+// fall in distinct banks).  One lane stores a full box with a TMA tensor
+// store, which writes whole lines and clips rows / columns outside C; the
+// next box goes to the other buffer while the first is read out.
+constexpr int EPI_BOX_BYTES = 4096;
+constexpr int EPI_BYTES = 4 * 2 * EPI_BOX_BYTES;  // four warps, two boxes each
+
+// Shared memory of the single-CTA kernel: stage ring, epilogue boxes,
+// control block (plus slack to align the base to 1024 bytes).
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + static_cast<int>(sizeof(Ctrl));
+
 template <int kKind>
-__device__ __forceinline__ void run_epilogue(const Params &p, Ctrl *ctrl, uint32_t tmem_base,
-                                             int warp, int lane, WaitCtl *wc)
+constexpr int box_cols()
 {
-    const int64_t num_tiles = p.tiles_m * p.tiles_n;
-    const Sched sc = schedule(p);
-    const uint32_t quarter = static_cast<uint32_t>(warp & 3);  // TMEM lanes this warp may read
-    uint32_t acc = 0, acc_phase = 0;
-    for (int64_t t = sc.t0; t < num_tiles; t += sc.dt) {
-        int64_t m0, n0;
-        tile_coords(t, p, m0, n0);
-        bool ok = wait_bounded(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, wc);
-        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const int64_t row = m0 + quarter * 32 + lane;
-        const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * BN;
+    return kKind == kF16 ? 64 : 32;
+}
+
+// C_old for one row and one box of columns (masked, zeros outside C).
+template <int kKind>
+__device__ __forceinline__ void load_old(const Params &p, int64_t row, int64_t col, float *old)
+{
+    constexpr int COLS = box_cols<kKind>();
+#pragma unroll
+    for (int e = 0; e < COLS; ++e) old[e] = 0.f;
+    if (row >= p.M) return;
+    if constexpr (kKind == kF16) {
+        const __half *crow = reinterpret_cast<const __half *>(p.C) + row * p.ldc;
+        if (p.vec_c && col + COLS - 1 < p.N) {
+#pragma unroll
+            for (int q = 0; q < COLS / 8; ++q) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(crow + col + q * 8);
+                const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h[e]);
+                    old[q * 8 + 2 * e] = f.x;
+                    old[q * 8 + 2 * e + 1] = f.y;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < COLS; ++e)
+                if (col + e < p.N) old[e] = __half2float(crow[col + e]);
+        }
+    } else {
+        const float *crow = reinterpret_cast<const float *>(p.C) + row * p.ldc;
+        if (p.vec_c && col + COLS - 1 < p.N) {
+#pragma unroll
+            for (int q = 0; q < COLS / 4; ++q) {
+                const float4 f = *reinterpret_cast<const float4 *>(crow + col + q * 4);
+                old[q * 4 + 0] = f.x;
+                old[q * 4 + 1] = f.y;
+                old[q * 4 + 2] = f.z;
+                old[q * 4 + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < COLS; ++e)
+                if (col + e < p.N) old[e] = crow[col + e];
+        }
+    }
+}
+
+// Drain one warp's 32 accumulator rows (TMEM address taddr, first row row0)
+// x BN columns from n0 into C.  nbox counts the boxes this warp has stored.
+template <int kKind>
+__device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *tmap_c,
+                                           uint32_t taddr, int64_t row0, int64_t n0,
+                                           uint32_t box_smem, int lane, uint32_t &nbox)
+{
+    const int64_t row = row0 + lane;
+    if (!p.tma_store) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             uint32_t r[32];
@@ -553,11 +600,81 @@ __device__ __forceinline__ void run_epilogue(const Params &p, Ctrl *ctrl, uint32
             ptx::tmem_ld_wait();
             store_chunk<kKind>(p, row, n0 + c * 32, r);
         }
+        return;
+    }
+    constexpr int COLS = box_cols<kKind>();
+#pragma unroll 1
+    for (int b = 0; b < BN / COLS; ++b) {
+        const int64_t col0 = n0 + b * COLS;
+        uint32_t r[COLS];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(taddr + b * COLS, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        if constexpr (COLS == 64)
+            ptx::tmem_ld_32x32b_x32(taddr + b * COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        ptx::tmem_ld_wait();
+        if (row0 >= p.M || col0 >= p.N) continue;  // warp-uniform: nothing of C here
+        float v[COLS];
+#pragma unroll
+        for (int e = 0; e < COLS; ++e) v[e] = p.alpha * __uint_as_float(r[e]);
+        if (p.beta != 0.f) {
+            float old[COLS];
+            load_old<kKind>(p, row, col0, old);
+#pragma unroll
+            for (int e = 0; e < COLS; ++e) v[e] = fmaf(p.beta, old[e], v[e]);
+        }
+        const uint32_t buf = box_smem + (nbox & 1u) * EPI_BOX_BYTES;
+        if (lane == 0 && nbox >= 2) ptx::bulk_wait_read<1>();  // this buffer's last store read it
+        __syncwarp();
+        const uint32_t rowbase = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint4 q;
+            if constexpr (kKind == kF16) {
+                __half2 h[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[j * 8 + 2 * e], v[j * 8 + 2 * e + 1]);
+                q = *reinterpret_cast<uint4 *>(h);
+            } else {
+                q = make_uint4(__float_as_uint(v[j * 4 + 0]), __float_as_uint(v[j * 4 + 1]),
+                               __float_as_uint(v[j * 4 + 2]), __float_as_uint(v[j * 4 + 3]));
+            }
+            ptx::st_shared_v4(rowbase + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u)) << 4), q);
+        }
+        ptx::fence_proxy_async_smem();  // make the box visible to the TMA engine
+        __syncwarp();
+        if (lane == 0) {
+            ptx::tma_store_2d(tmap_c, buf, static_cast<int32_t>(col0), static_cast<int32_t>(row0));
+            ptx::bulk_commit();
+        }
+        ++nbox;
+    }
+}
+
+template <int kKind>
+__device__ __forceinline__ void run_epilogue(const Params &p, const CUtensorMap *tmap_c, Ctrl *ctrl,
+                                             uint32_t tmem_base, uint32_t epi_smem, int warp,
+                                             int lane, WaitCtl *wc)
+{
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const Sched sc = schedule(p);
+    const uint32_t quarter = static_cast<uint32_t>(warp & 3);  // TMEM lanes this warp may read
+    uint32_t acc = 0, acc_phase = 0, nbox = 0;
+    for (int64_t t = sc.t0; t < num_tiles; t += sc.dt) {
+        int64_t m0, n0;
+        tile_coords(t, p, m0, n0);
+        bool ok = wait_bounded(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, wc);
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * BN;
+        drain_rows<kKind>(p, tmap_c, taddr, m0 + quarter * 32, n0,
+                          epi_smem + quarter * 2 * EPI_BOX_BYTES, lane, nbox);
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_addr(&ctrl->tmem_empty[acc]));
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) ptx::bulk_wait<0>();  // stores done before the CTA leaves
 }
 
 // ---- split-K: the partial sums of a tile meet in distributed shared memory
@@ -667,13 +784,14 @@ constexpr int cta_threads()
 template <int kKind, bool kTma>
 __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                     const __grid_constant__ CUtensorMap tmap_b, const Params p)
+                     const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_c, const Params p)
 {
     constexpr int kMmaWarp = producer_warps<kTma>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + STAGES * STAGE_BYTES);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -686,6 +804,7 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
             ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_empty[a]), 4 * 32);
         }
         ptx::mbar_init(ptx::smem_addr(&ctrl->mma_done), 1);
+        ptx::mbar_init(ptx::smem_addr(&ctrl->never), 1);
         ctrl->wait.abort = 0;
         ctrl->wait.limit_ns = p.wait_limit_ns;
         ptx::fence_mbarrier_init();
@@ -694,6 +813,7 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
         ptx::prefetch_tmap(&tmap_a);
         ptx::prefetch_tmap(&tmap_b);
     }
+    if (p.tma_store && warp == kMmaWarp + 1 && lane == 0) ptx::prefetch_tmap(&tmap_c);
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_addr(&ctrl->tmem_base), TMEM_COLS);
         ptx::tmem_relinquish();
@@ -717,7 +837,8 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
         if (p.splitk > 1)
             splitk_push(p, ctrl, tmem_base, smem_base, warp, lane, wc);
         else
-            run_epilogue<kKind>(p, ctrl, tmem_base, warp, lane, wc);
+            run_epilogue<kKind>(p, &tmap_c, ctrl, tmem_base, smem_base + STAGES * STAGE_BYTES, warp,
+                                lane, wc);
     }
 
     if (p.splitk > 1) {  // uniform over the cluster
@@ -768,11 +889,13 @@ struct PairCtrl {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
+    uint64_t never;  // test hook: a barrier nothing arrives at
     WaitCtl wait;
     uint32_t tmem_base;
 };
 
-constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + static_cast<int>(sizeof(PairCtrl));
+constexpr int PAIR_SMEM_BYTES =
+    PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES + 1024 + static_cast<int>(sizeof(PairCtrl));
 
 template <int kKind>
 constexpr uint32_t pair_idesc()
@@ -791,7 +914,6 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
     uint32_t stage = 0, phase = 0;
     uint32_t issued = 0, issued_phase = 0;
     bool ok = true;
-    bool stall = p.inject_stall != 0;  // test hook: never deliver the first stage
     for (int64_t t = cluster; ok && t < num_tiles; t += clusters) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0, PAIR_BM);
@@ -799,14 +921,6 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
             if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
                 ok = false;
                 break;
-            }
-            if (stall) {
-                stall = false;
-                if (++stage == PAIR_STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                continue;
             }
             const uint32_t full_local = ptx::smem_addr(&ctrl->full[stage]);
             const uint32_t full = ptx::mapa(full_local, 0);  // the even CTA's barrier
@@ -849,7 +963,8 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-    bool ok = true;
+    // test hook: wait on a barrier nothing arrives at, so the wait runs out
+    bool ok = !p.inject_stall || wait_bounded(ptx::smem_addr(&ctrl->never), 0, wc);
     for (int64_t t = cluster; ok && t < num_tiles; t += clusters) {
         if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u,
                                   wc)) {
@@ -892,14 +1007,14 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
 }
 
 template <int kKind>
-__device__ __forceinline__ void pair_epilogue(const Params &p, PairCtrl *ctrl, uint32_t tmem_base,
-                                              uint32_t rank, int warp, int lane,
-                                              WaitCtl *wc)
+__device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap *tmap_c,
+                                              PairCtrl *ctrl, uint32_t tmem_base, uint32_t epi_smem,
+                                              uint32_t rank, int warp, int lane, WaitCtl *wc)
 {
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
     const uint32_t quarter = static_cast<uint32_t>(warp & 3);
-    uint32_t acc = 0, acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0, nbox = 0;
     for (int64_t t = cluster; t < num_tiles; t += clusters) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0, PAIR_BM);
@@ -907,16 +1022,9 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, PairCtrl *ctrl, u
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
-        const int64_t row = m0 + rank * 128 + quarter * 32 + lane;
         const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            __syncwarp();
-            ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
-            ptx::tmem_ld_wait();
-            store_chunk<kKind>(p, row, n0 + c * 32, r);
-        }
+        drain_rows<kKind>(p, tmap_c, taddr, m0 + rank * 128 + quarter * 32, n0,
+                          epi_smem + quarter * 2 * EPI_BOX_BYTES, lane, nbox);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0)
@@ -924,17 +1032,19 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, PairCtrl *ctrl, u
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) ptx::bulk_wait<0>();  // stores done before the CTA leaves
 }
 
 template <int kKind>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     umma_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                     const __grid_constant__ CUtensorMap tmap_b, const Params p)
+                     const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_c, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    PairCtrl *ctrl = reinterpret_cast<PairCtrl *>(smem + PAIR_STAGES * PAIR_STAGE_BYTES);
+    PairCtrl *ctrl = reinterpret_cast<PairCtrl *>(smem + PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ptx::cluster_ctarank();
 
@@ -948,6 +1058,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_empty[a]), 8);
         }
         ptx::mbar_init(ptx::smem_addr(&ctrl->mma_done), 1);
+        ptx::mbar_init(ptx::smem_addr(&ctrl->never), 1);
         ctrl->wait.abort = 0;
         ctrl->wait.limit_ns = p.wait_limit_ns;
         ptx::fence_mbarrier_init();
@@ -956,6 +1067,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         ptx::prefetch_tmap(&tmap_a);
         ptx::prefetch_tmap(&tmap_b);
     }
+    if (p.tma_store && warp == 2 && lane == 0) ptx::prefetch_tmap(&tmap_c);
     if (warp == 1) {
         ptx::tmem_alloc_pair(ptx::smem_addr(&ctrl->tmem_base), TMEM_COLS);
         ptx::tmem_relinquish_pair();
@@ -972,7 +1084,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) pair_mma<kKind>(p, smem_base, ctrl, tmem_base, wc);
     } else {
-        pair_epilogue<kKind>(p, ctrl, tmem_base, rank, warp, lane, wc);
+        pair_epilogue<kKind>(p, &tmap_c, ctrl, tmem_base, smem_base + PAIR_STAGES * PAIR_STAGE_BYTES,
+                             rank, warp, lane, wc);
     }
 
     __syncwarp();  // the barrier below is warp-aligned: reconverge lane 0 with the rest
@@ -1020,8 +1133,8 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t
 }
 
 template <int kKind, bool kTma>
-bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, cudaStream_t stream,
-            const DeviceInfo &dev)
+bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const Params &p,
+            cudaStream_t stream, const DeviceInfo &dev)
 {
     if (cudaFuncSetAttribute(umma_gemm_kernel<kKind, kTma>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
@@ -1029,7 +1142,7 @@ bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, cudaS
     const int64_t tiles = p.tiles_m * p.tiles_n;
     const int64_t grid = tiles < dev.sm_count ? tiles : dev.sm_count;
     umma_gemm_kernel<kKind, kTma>
-        <<<static_cast<unsigned>(grid), cta_threads<kTma>(), SMEM_BYTES, stream>>>(ma, mb, p);
+        <<<static_cast<unsigned>(grid), cta_threads<kTma>(), SMEM_BYTES, stream>>>(ma, mb, mc, p);
     return true;
 }
 
@@ -1069,7 +1182,8 @@ int pair_clusters()
 }
 
 template <int kKind>
-bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, cudaStream_t stream)
+bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const Params &p,
+                 cudaStream_t stream)
 {
     const int clusters = pair_clusters<kKind>();
     if (clusters <= 0) return false;
@@ -1087,7 +1201,7 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind>, ma, mb, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind>, ma, mb, mc, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -1183,8 +1297,8 @@ int choose_splitk(const Params &p, int sm_count)
 }
 
 template <int kKind>
-bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p,
-                   cudaStream_t stream)
+bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
+                   const Params &p, cudaStream_t stream)
 {
     if (cudaFuncSetAttribute(umma_gemm_kernel<kKind, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
@@ -1203,7 +1317,7 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, umma_gemm_kernel<kKind, true>, ma, mb, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, umma_gemm_kernel<kKind, true>, ma, mb, mc, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -1228,21 +1342,21 @@ const char *splitk_name(int kind, int s)
 // mb_pair: B with 128-row boxes.
 template <int kKind>
 const char *dispatch_tma(const Params &p, const CUtensorMap &ma, const CUtensorMap &mb,
-                         const CUtensorMap *mb_pair, cudaStream_t stream, const DeviceInfo &dev,
-                         const char *pair_name, const char *single_name)
+                         const CUtensorMap *mb_pair, const CUtensorMap &mc, cudaStream_t stream,
+                         const DeviceInfo &dev, const char *pair_name, const char *single_name)
 {
     const int S = choose_splitk<kKind>(p, dev.sm_count);
     if (S > 1) {
         Params ps = p;
         ps.splitk = S;
-        if (launch_splitk<kKind>(ma, mb, ps, stream)) return splitk_name(kKind, S);
+        if (launch_splitk<kKind>(ma, mb, mc, ps, stream)) return splitk_name(kKind, S);
     }
     if (mb_pair && p.M > BM) {
         Params pp = p;
         pp.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
-        if (launch_pair<kKind>(ma, *mb_pair, pp, stream)) return pair_name;
+        if (launch_pair<kKind>(ma, *mb_pair, mc, pp, stream)) return pair_name;
     }
-    return launch<kKind, true>(ma, mb, p, stream, dev) ? single_name : nullptr;
+    return launch<kKind, true>(ma, mb, mc, p, stream, dev) ? single_name : nullptr;
 }
 
 }  // namespace
@@ -1251,8 +1365,12 @@ const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, con
                                int64_t lda, const uint16_t *B, int64_t ldb, float beta,
                                uint16_t *C, int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
 {
-    const Params p = make_params(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, Traits<kF16>::BK,
-                                 aligned16(C) && (ldc % 8 == 0));
+    Params p = make_params(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, Traits<kF16>::BK,
+                           aligned16(C) && (ldc % 8 == 0));
+    CUtensorMap mc{};
+    p.tma_store = (p.vec_c && make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, ldc * 2,
+                                       box_cols<kF16>(), 32, CU_TENSOR_MAP_SWIZZLE_128B))
+                      ? 1 : 0;
     // TMA needs 16-byte aligned bases and row pitches.
     const bool tma = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
     CUtensorMap ma{}, mb{}, mbp{};
@@ -1263,18 +1381,22 @@ const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, con
                  CU_TENSOR_MAP_SWIZZLE_128B)) {
         const bool pair_map = make_map(&mbp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2,
                                        Traits<kF16>::BK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-        return dispatch_tma<kF16>(p, ma, mb, pair_map ? &mbp : nullptr, stream, dev,
+        return dispatch_tma<kF16>(p, ma, mb, pair_map ? &mbp : nullptr, mc, stream, dev,
                                   "umma_f16_tn_pair_256x256x64_tma", "umma_f16_tn_128x256x64_tma");
     }
-    return launch<kF16, false>(ma, mb, p, stream, dev) ? "umma_f16_tn_128x256x64_ldst" : nullptr;
+    return launch<kF16, false>(ma, mb, mc, p, stream, dev) ? "umma_f16_tn_128x256x64_ldst" : nullptr;
 }
 
 const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                              int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                              int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
 {
-    const Params p = make_params(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, Traits<kTF32>::BK,
-                                 aligned16(C) && (ldc % 4 == 0));
+    Params p = make_params(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, Traits<kTF32>::BK,
+                           aligned16(C) && (ldc % 4 == 0));
+    CUtensorMap mc{};
+    p.tma_store = (p.vec_c && make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, ldc * 4,
+                                       box_cols<kTF32>(), 32, CU_TENSOR_MAP_SWIZZLE_128B))
+                      ? 1 : 0;
     const bool tma = aligned16(A) && aligned16(B) && (lda * 4) % 16 == 0 && (ldb * 4) % 16 == 0;
     CUtensorMap ma{}, mb{};
     if (tma &&
@@ -1283,10 +1405,10 @@ const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const
         make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK,
                  CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)) {
         // TF32's B boxes are 32 x 32 for both kernels: one map serves both
-        return dispatch_tma<kTF32>(p, ma, mb, &mb, stream, dev, "umma_tf32_pair_256x256x32_tma",
+        return dispatch_tma<kTF32>(p, ma, mb, &mb, mc, stream, dev, "umma_tf32_pair_256x256x32_tma",
                                    "umma_tf32_128x256x32_tma");
     }
-    return launch<kTF32, false>(ma, mb, p, stream, dev) ? "umma_tf32_128x256x32_ldst" : nullptr;
+    return launch<kTF32, false>(ma, mb, mc, p, stream, dev) ? "umma_tf32_128x256x32_ldst" : nullptr;
 }
 
 void umma_inject_stall(uint64_t wait_limit_ns)

@@ -133,8 +133,8 @@ int dgemm_device_status(int clear);
 /*
  * dgemm_test_inject_stall -- TEST HOOK, not for applications.  Arms a one-shot
  * fault for the next gemm_tf32 / gemm_f16_tn launch made by the calling host
- * thread: its producers never deliver the first pipeline stage, and every
- * wait of that launch is bounded by wait_limit_ns (0 means 1 ns) instead of
+ * thread: its MMA issuer first waits on a barrier that nothing arrives at,
+ * and every wait of that launch is bounded by wait_limit_ns (0 means 1 ns) instead of
  * the default 4 s.  The launch then ends by itself, with DGEMM_ERR_TIMEOUT in
  * the device status word (see dgemm_device_status) and C left unspecified;
  * the CUDA context stays usable.  Always returns DGEMM_OK.  Source: none on

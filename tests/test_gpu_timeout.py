@@ -1,7 +1,7 @@
 """Failure detection on the GPU without a fault: the bounded mbarrier waits.
 
-A test-only hook makes the next tensor-core launch withhold its first
-pipeline stage, so the MMA issuer's wait (and then every other role's) runs
+A test-only hook makes the next tensor-core launch's MMA issuer wait on a
+barrier nothing arrives at, so its wait (and then every other role's) runs
 out after a short limit.  The kernel must end by itself, record
 DGEMM_ERR_TIMEOUT in the device status word, release its resources, and leave
 the context usable: the next ordinary call is correct."""
