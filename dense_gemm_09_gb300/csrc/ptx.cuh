@@ -67,6 +67,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+__device__ __forceinline__ void cp_async_commit_group()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 // cp.async (non-bulk) arrival: the mbarrier gets one arrival once all of this
 // thread's prior cp.async copies have landed (the pending count is not
 // incremented first, so the barrier's expected count must include it).

@@ -380,6 +380,93 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
     }
 }
 
+// cp.async producer for 4-byte operands (TF32) that TMA cannot describe:
+// the same swizzled K-major tiles as run_reg_producer, but every element is a
+// 4-byte asynchronous copy (zero-filled outside M, N, K), so each thread keeps
+// kInFlight stages of copies outstanding instead of waiting for its loads.
+// A stage's "full" barrier gets this thread's arrival once its copies of
+// that stage have landed (cp.async.wait_group) and been fenced to the async
+// proxy.  kInFlight < STAGES, so the MMA can always drain the oldest stage.
+__device__ __forceinline__ void cp_async4_zfill(uint32_t dst, const void *src, bool ok)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(ok ? 4 : 0)
+                 : "memory");
+}
+
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait_pending()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+__device__ __forceinline__ void run_cpasync_producer(const Params &p, uint32_t smem_base, Ctrl *ctrl,
+                                                     int ptid, WaitCtl *wc)
+{
+    using T = Traits<kTF32>;
+    constexpr int BK = T::BK;
+    constexpr int kInFlight = 3;
+    static_assert(kInFlight < STAGES, "the oldest stage must be released before a slot is reused");
+    const float *__restrict__ A = static_cast<const float *>(p.A);
+    const float *__restrict__ B = static_cast<const float *>(p.B);
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const Sched sc = schedule(p);
+    uint32_t stage = 0, phase = 0;
+    uint32_t pending[kInFlight];
+    int npending = 0;
+    bool ok = true;
+    for (int64_t t = sc.t0; ok && t < num_tiles; t += sc.dt) {
+        int64_t m0, n0;
+        tile_coords(t, p, m0, n0);
+        for (int64_t kb = sc.kb0; kb < sc.kb1; ++kb) {
+            if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
+                ok = false;
+                break;
+            }
+            const int64_t k0 = kb * BK;
+            const uint32_t sa = smem_base + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_TILE_BYTES;
+            // A tile: BM rows x BK; consecutive threads take consecutive k
+#pragma unroll 8
+            for (int i = 0; i < BM * BK / 128; ++i) {
+                const int idx = ptid + i * 128;
+                const int r = idx / BK, c = idx % BK;
+                const int64_t gm = m0 + r, gk = k0 + c;
+                const bool in = gm < p.M && gk < p.K;
+                cp_async4_zfill(sa + sw128_offset(r, c * 4), in ? A + gm * p.lda + gk : A, in);
+            }
+            // B tile (stored K x N): consecutive threads take consecutive n;
+            // staged K-major (row n holds BK consecutive k)
+#pragma unroll 8
+            for (int i = 0; i < BN * BK / 128; ++i) {
+                const int idx = ptid + i * 128;
+                const int n = idx % BN, k = idx / BN;
+                const int64_t gn = n0 + n, gk = k0 + k;
+                const bool in = gn < p.N && gk < p.K;
+                cp_async4_zfill(sb + sw128_offset(n, k * 4), in ? B + gk * p.ldb + gn : B, in);
+            }
+            ptx::cp_async_commit_group();
+            pending[npending++] = stage;
+            if (npending == kInFlight) {
+                cp_async_wait_pending<kInFlight - 1>();  // the oldest stage's copies landed
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(ptx::smem_addr(&ctrl->full[pending[0]]));
+#pragma unroll
+                for (int q = 0; q + 1 < kInFlight; ++q) pending[q] = pending[q + 1];
+                --npending;
+            }
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // release what is still in flight, oldest first (also on the way out of
+    // an abort: every copy this thread issued lands before it leaves)
+    cp_async_wait_pending<0>();
+    ptx::fence_proxy_async_smem();
+    for (int q = 0; q < npending; ++q) ptx::mbar_arrive(ptx::smem_addr(&ctrl->full[pending[q]]));
+}
+
 template <int kKind, bool kTma>
 __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctrl *ctrl,
                                         uint32_t tmem_base, WaitCtl *wc)
@@ -828,6 +915,8 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
     if (warp < kMmaWarp) {
         if constexpr (kTma) {
             if (lane == 0) run_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, wc);
+        } else if constexpr (kKind == kTF32) {
+            run_cpasync_producer(p, smem_base, ctrl, threadIdx.x, wc);
         } else {
             run_reg_producer<kKind>(p, smem_base, ctrl, threadIdx.x, wc);
         }
@@ -1408,7 +1497,7 @@ const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const
         return dispatch_tma<kTF32>(p, ma, mb, &mb, mc, stream, dev, "umma_tf32_pair_256x256x32_tma",
                                    "umma_tf32_128x256x32_tma");
     }
-    return launch<kTF32, false>(ma, mb, mc, p, stream, dev) ? "umma_tf32_128x256x32_ldst" : nullptr;
+    return launch<kTF32, false>(ma, mb, mc, p, stream, dev) ? "umma_tf32_128x256x32_cpasync" : nullptr;
 }
 
 void umma_inject_stall(uint64_t wait_limit_ns)

@@ -18,7 +18,8 @@ CASES = [
     ("f16_tn", (256, 512, 256), (0, 0, 0), "_pair_"),     # CTA-pair kernel
     ("tf32", (256, 512, 256), (0, 0, 0), "_pair_"),
     ("f16_tn", (128, 512, 256), (0, 0, 0), "_128x256x64_tma"),   # single-CTA kernel
-    ("tf32", (100, 260, 36), (1, 0, 0), "_ldst"),         # register-path producer
+    ("tf32", (100, 260, 36), (1, 0, 0), "_cpasync"),      # cp.async producer (unaligned TF32)
+    ("f16_tn", (100, 260, 36), (1, 0, 0), "_ldst"),       # register-path producer (unaligned FP16)
     ("f16_tn", (100, 1000, 2048), (0, 0, 0), "_splitk"),  # split-K cluster kernel
 ]
 
