@@ -10,6 +10,8 @@ an exception is raised.
     gemm_tf32(A, B, C, alpha, beta)    same, TF32 tensor cores   (FP32 in / out)
     gemm_f16_tn(A, B, C, alpha, beta)  C = alpha*A@B.T + beta*C  (FP16 in / out,
                                                                    FP32 accumulate)
+    gemm_f16_nn(A, B, C, alpha, beta)  C = alpha*A@B + beta*C    (FP16, B is K x N)
+    gemm_bf16_tn / gemm_bf16_nn         the same with bfloat16
 
 Matrices are 2-D tensors with unit column stride; a row stride larger than
 the width is passed on as the leading dimension.  C is updated in place and
@@ -55,7 +57,8 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         i64, f32, vp, ci = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
         sig = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
-        for name in ("gemm_f32", "gemm_tf32", "gemm_f16_tn"):
+        for name in ("gemm_f32", "gemm_tf32", "gemm_f16_tn", "gemm_f16_nn", "gemm_bf16_tn",
+                     "gemm_bf16_nn"):
             fn = getattr(L, name)
             fn.argtypes = sig
             fn.restype = ci
@@ -140,14 +143,33 @@ def gemm_tf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
     return _nn("gemm_tf32", A, B, C, alpha, beta, stream)
 
 
-def gemm_f16_tn(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
-    """C = alpha * A @ B.T + beta * C; A: M x K, B: N x K, C: M x N, all f16."""
-    pa, lda = _mat(A, "A", torch.float16)
-    pb, ldb = _mat(B, "B", torch.float16)
-    pc, ldc = _mat(C, "C", torch.float16)
+def _gemm16(name, dtype, tn, A, B, C, alpha, beta, stream):
+    pa, lda = _mat(A, "A", dtype)
+    pb, ldb = _mat(B, "B", dtype)
+    pc, ldc = _mat(C, "C", dtype)
     M, K = A.shape
-    N, K2 = B.shape
+    N, K2 = B.shape if tn else (B.shape[1], B.shape[0])
     if K2 != K or tuple(C.shape) != (M, N):
         raise ValueError("shape mismatch: A %s, B %s, C %s" % (tuple(A.shape), tuple(B.shape), tuple(C.shape)))
-    _call("gemm_f16_tn", M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, stream)
+    _call(name, M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, stream)
     return C
+
+
+def gemm_f16_tn(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B.T + beta * C; A: M x K, B: N x K, C: M x N, all f16."""
+    return _gemm16("gemm_f16_tn", torch.float16, True, A, B, C, alpha, beta, stream)
+
+
+def gemm_f16_nn(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B + beta * C; A: M x K, B: K x N, C: M x N, all f16."""
+    return _gemm16("gemm_f16_nn", torch.float16, False, A, B, C, alpha, beta, stream)
+
+
+def gemm_bf16_tn(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B.T + beta * C with bfloat16 A, B (N x K) and C."""
+    return _gemm16("gemm_bf16_tn", torch.bfloat16, True, A, B, C, alpha, beta, stream)
+
+
+def gemm_bf16_nn(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B + beta * C with bfloat16 A, B (K x N) and C."""
+    return _gemm16("gemm_bf16_nn", torch.bfloat16, False, A, B, C, alpha, beta, stream)

@@ -99,19 +99,55 @@ extern "C" int gemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const flo
     DeviceInfo dev;
     if ((st = check_device(dev)) != DGEMM_OK) return st;
     if (K == 0 || alpha == 0.f) return finish(launch_scale_f32(M, N, beta, C, ldc, stream));
-    return finish(launch_umma_tf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev));
+    return finish(launch_umma(kUmmaTF32NN, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev));
 }
+
+namespace {
+
+// The 16-bit entry points: kind selects the input / output type and the
+// layout of B (TN: stored N x K, ldb >= K; NN: stored K x N, ldb >= N).
+int gemm_16bit(int kind, bool bf16, bool nn, int64_t M, int64_t N, int64_t K, float alpha,
+               const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, float beta,
+               uint16_t *C, int64_t ldc, cudaStream_t stream)
+{
+    int st = validate(M, N, K, alpha, A, lda, B, ldb, nn ? N : K, C, ldc);
+    if (st != DGEMM_OK || M == 0 || N == 0) return st;
+    DeviceInfo dev;
+    if ((st = check_device(dev)) != DGEMM_OK) return st;
+    if (K == 0 || alpha == 0.f)
+        return finish(bf16 ? launch_scale_bf16(M, N, beta, C, ldc, stream)
+                           : launch_scale_f16(M, N, beta, C, ldc, stream));
+    return finish(launch_umma(kind, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev));
+}
+
+}  // namespace
 
 extern "C" int gemm_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
                            int64_t lda, const uint16_t *B, int64_t ldb, float beta, uint16_t *C,
                            int64_t ldc, cudaStream_t stream)
 {
-    int st = validate(M, N, K, alpha, A, lda, B, ldb, K, C, ldc);
-    if (st != DGEMM_OK || M == 0 || N == 0) return st;
-    DeviceInfo dev;
-    if ((st = check_device(dev)) != DGEMM_OK) return st;
-    if (K == 0 || alpha == 0.f) return finish(launch_scale_f16(M, N, beta, C, ldc, stream));
-    return finish(launch_umma_f16_tn(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev));
+    return gemm_16bit(kUmmaF16TN, false, false, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+extern "C" int gemm_f16_nn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
+                           int64_t lda, const uint16_t *B, int64_t ldb, float beta, uint16_t *C,
+                           int64_t ldc, cudaStream_t stream)
+{
+    return gemm_16bit(kUmmaF16NN, false, true, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+extern "C" int gemm_bf16_tn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
+                            int64_t lda, const uint16_t *B, int64_t ldb, float beta, uint16_t *C,
+                            int64_t ldc, cudaStream_t stream)
+{
+    return gemm_16bit(kUmmaBF16TN, true, false, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+extern "C" int gemm_bf16_nn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
+                            int64_t lda, const uint16_t *B, int64_t ldb, float beta, uint16_t *C,
+                            int64_t ldc, cudaStream_t stream)
+{
+    return gemm_16bit(kUmmaBF16NN, true, true, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
 }
 
 extern "C" const char *dgemm_status_string(int status)

@@ -25,6 +25,8 @@ const char *launch_scale_f32(int64_t M, int64_t N, float beta, float *C, int64_t
                              cudaStream_t stream);
 const char *launch_scale_f16(int64_t M, int64_t N, float beta, uint16_t *C, int64_t ldc,
                              cudaStream_t stream);
+const char *launch_scale_bf16(int64_t M, int64_t N, float beta, uint16_t *C, int64_t ldc,
+                              cudaStream_t stream);
 
 struct DeviceInfo {
     int major = 0, minor = 0;
@@ -32,15 +34,14 @@ struct DeviceInfo {
     int max_smem_optin = 0;
 };
 
-// Tensor-core paths.  Return nullptr if the launch could not be prepared
-// (e.g. the driver's tensor-map encoder is unavailable).
-const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
-                               int64_t lda, const uint16_t *B, int64_t ldb, float beta,
-                               uint16_t *C, int64_t ldc, cudaStream_t stream,
-                               const DeviceInfo &dev);
-const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
-                             int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-                             int64_t ldc, cudaStream_t stream, const DeviceInfo &dev);
+// Tensor-core paths: operand kinds (TN = B stored N x K, NN = B stored K x N).
+enum UmmaKind { kUmmaF16TN = 0, kUmmaTF32NN = 1, kUmmaBF16TN = 2, kUmmaF16NN = 3, kUmmaBF16NN = 4 };
+
+// Returns nullptr if the launch could not be prepared (e.g. the driver's
+// tensor-map encoder is unavailable).
+const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+                        int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc,
+                        cudaStream_t stream, const DeviceInfo &dev);
 
 // Device status word of the tensor-core kernels (see dgemm_device_status).
 int umma_read_status(int clear);

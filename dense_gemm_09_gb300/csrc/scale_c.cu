@@ -4,6 +4,7 @@
 // coalesced along each row.
 #include <cstdint>
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -35,6 +36,17 @@ __global__ void scale_f16_kernel(int64_t M, int64_t N, float beta, __half *__res
     }
 }
 
+__global__ void scale_bf16_kernel(int64_t M, int64_t N, float beta, __nv_bfloat16 *__restrict__ C,
+                                  int64_t ldc)
+{
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+        __nv_bfloat16 *row = C + m * ldc;
+        for (int64_t n = threadIdx.x; n < N; n += blockDim.x)
+            row[n] = (beta == 0.f) ? __float2bfloat16_rn(0.f)
+                                   : __float2bfloat16_rn(beta * __bfloat162float(row[n]));
+    }
+}
+
 unsigned grid_for(int64_t M)
 {
     return static_cast<unsigned>(M < 65536 ? M : 65536);
@@ -55,6 +67,14 @@ const char *launch_scale_f16(int64_t M, int64_t N, float beta, uint16_t *C, int6
     scale_f16_kernel<<<grid_for(M), kThreads, 0, stream>>>(M, N, beta,
                                                            reinterpret_cast<__half *>(C), ldc);
     return "scale_c_f16";
+}
+
+const char *launch_scale_bf16(int64_t M, int64_t N, float beta, uint16_t *C, int64_t ldc,
+                              cudaStream_t stream)
+{
+    scale_bf16_kernel<<<grid_for(M), kThreads, 0, stream>>>(M, N, beta,
+                                                            reinterpret_cast<__nv_bfloat16 *>(C), ldc);
+    return "scale_c_bf16";
 }
 
 }  // namespace dgemm

@@ -41,10 +41,12 @@
 // own copies and MMAs in flight, and the CTA releases its TMEM and exits.
 #include <cstdint>
 #include <mutex>
+#include <string>
 #include <type_traits>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -70,32 +72,81 @@ constexpr int kGroupN = 8;                         // tile-order group width
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s, default wait bound
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
 
-enum { kF16 = 0, kTF32 = 1 };
+// Operand kinds.  TN: B stored N x K (K-major); NN: B stored K x N
+// (N-major).  TF32 reads FP32 storage; all kinds accumulate in FP32.
+enum { kF16 = 0, kTF32 = 1, kBF16 = 2, kF16NN = 3, kBF16NN = 4 };
 
 template <int kKind>
-struct Traits;
-template <>
-struct Traits<kF16> {
-    static constexpr int kElem = 2;
-    static constexpr int BK = ROW_BYTES / kElem;  // 64
-    static constexpr int UMMA_K = 16;             // 32 bytes of K per MMA
-    // D = f32 (bits 4-5 = 1), A = B = f16 (0), both K-major, N >> 3, M >> 4.
-    static constexpr uint32_t kIdesc =
-        (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
-    static constexpr uint32_t kIdescKMajorB = kIdesc;
-};
-template <>
-struct Traits<kTF32> {
-    static constexpr int kElem = 4;
-    static constexpr int BK = ROW_BYTES / kElem;  // 32
-    static constexpr int UMMA_K = 8;              // 32 bytes of K per MMA
-    // D = f32, A = B = tf32 (code 2), A K-major, B N-major (bit 16).
-    static constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (1u << 16) |
+struct Traits {
+    static constexpr bool kTf32 = kKind == kTF32;
+    static constexpr int kElem = kTf32 ? 4 : 2;         // bytes per A / B / C element
+    static constexpr int BK = ROW_BYTES / kElem;         // K per stage: one 128-byte row
+    static constexpr int UMMA_K = 32 / kElem;            // K per MMA: 32 bytes
+    static constexpr bool kBF = kKind == kBF16 || kKind == kBF16NN;
+    // B stored K x N (N-major) rather than N x K
+    static constexpr bool kBNMajor = kKind == kTF32 || kKind == kF16NN || kKind == kBF16NN;
+    // operand format code of the instruction descriptor: f16 0, bf16 1, tf32 2
+    static constexpr uint32_t kFmt = kTf32 ? 2u : (kBF ? 1u : 0u);
+    // N-major B in shared memory: boxes of 128 bytes of columns x BK rows.
+    // 16-bit: 128-byte swizzle of 16-byte chunks, 8-row K groups 1 KB apart;
+    // 32-bit: the 32-byte-chunk swizzle, read as 4-row halves 512 B apart.
+    static constexpr int kNBox = ROW_BYTES / kElem;       // columns per box: 64 or 32
+    static constexpr uint32_t kNBoxBytes = BK * ROW_BYTES;  // 8 KB or 4 KB
+    static constexpr uint32_t kNLayout = kTf32 ? ptx::kSw128A32 : ptx::kSw128;
+    static constexpr uint32_t kNSbo = kTf32 ? 512u : 1024u;
+    static constexpr uint32_t kNStep = UMMA_K * ROW_BYTES;  // bytes of one MMA's K rows
+    // D = f32 (bits 4-5 = 1), A / B formats, B major (bit 16), N >> 3, M >> 4
+    static constexpr uint32_t kIdesc = (1u << 4) | (kFmt << 7) | (kFmt << 10) |
+                                       ((kBNMajor ? 1u : 0u) << 16) |
                                        (static_cast<uint32_t>(BN >> 3) << 17) |
                                        (static_cast<uint32_t>(BM >> 4) << 24);
-    // B staged K-major (the register-path producer transposes it).
+    // B staged K-major (the register-path producers transpose it)
     static constexpr uint32_t kIdescKMajorB = kIdesc & ~(1u << 16);
 };
+
+// 2-byte output conversions (f16 or bf16), round to nearest even.
+template <bool kBF>
+__device__ __forceinline__ uint32_t pack2(float a, float b)
+{
+    if constexpr (kBF) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+}
+
+template <bool kBF>
+__device__ __forceinline__ float2 unpack2(uint32_t u)
+{
+    if constexpr (kBF)
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+    else
+        return __half22float2(*reinterpret_cast<const __half2 *>(&u));
+}
+
+template <bool kBF>
+__device__ __forceinline__ float load1(const uint16_t *p)
+{
+    const uint16_t u = *p;
+    if constexpr (kBF)
+        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(&u));
+    else
+        return __half2float(*reinterpret_cast<const __half *>(&u));
+}
+
+template <bool kBF>
+__device__ __forceinline__ uint16_t round1(float v)
+{
+    if constexpr (kBF) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        return *reinterpret_cast<const uint16_t *>(&h);
+    } else {
+        const __half h = __float2half_rn(v);
+        return *reinterpret_cast<const uint16_t *>(&h);
+    }
+}
 
 // Per-CTA wait control: the abort flag every role polls and the wait limit.
 struct WaitCtl {
@@ -262,15 +313,15 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
             const uint32_t sb = sa + A_TILE_BYTES;
             const int32_t kc = static_cast<int32_t>(kb * T::BK);
             ptx::tma_load_2d(sa, tmap_a, full, kc, static_cast<int32_t>(m0));
-            if constexpr (kKind == kF16) {
+            if constexpr (!T::kBNMajor) {
                 ptx::tma_load_2d(sb, tmap_b, full, kc, static_cast<int32_t>(n0));
             } else {
-                // B is N-major: eight 32(N) x 32(K) boxes, one 4 KB column
-                // each, written with the 32-byte-atom 128-byte swizzle.
+                // B is N-major: boxes of 128 bytes of columns x BK rows, one
+                // swizzle column each (see Traits)
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-                    ptx::tma_load_2d(sb + c * 4096, tmap_b, full,
-                                     static_cast<int32_t>(n0 + c * 32), kc);
+                for (int c = 0; c < BN / T::kNBox; ++c)
+                    ptx::tma_load_2d(sb + c * T::kNBoxBytes, tmap_b, full,
+                                     static_cast<int32_t>(n0 + c * T::kNBox), kc);
             }
             issued |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -317,7 +368,7 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
                                                  int ptid, WaitCtl *wc)
 {
     using T = Traits<kKind>;
-    using E = typename std::conditional<kKind == kF16, uint16_t, uint32_t>::type;
+    using E = typename std::conditional<T::kElem == 2, uint16_t, uint32_t>::type;
     constexpr int BK = T::BK;
     constexpr int kBatch = 8;
     const E *__restrict__ A = static_cast<const E *>(p.A);
@@ -354,7 +405,7 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u) {
                     const int idx = ptid + (i0 + u) * 128;
-                    if constexpr (kKind == kF16) {  // B stored N x K: walk k
+                    if constexpr (!T::kBNMajor) {  // B stored N x K: walk k
                         const int64_t gn = n0 + idx / BK, gk = k0 + idx % BK;
                         v[u] = (gn < p.N && gk < p.K) ? B[gn * p.ldb + gk] : E(0);
                     } else {  // B stored K x N: walk n (coalesced), transpose into smem
@@ -365,8 +416,8 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u) {
                     const int idx = ptid + (i0 + u) * 128;
-                    const int n = (kKind == kF16) ? idx / BK : idx % BN;
-                    const int k = (kKind == kF16) ? idx % BK : idx / BN;
+                    const int n = !T::kBNMajor ? idx / BK : idx % BN;
+                    const int k = !T::kBNMajor ? idx % BK : idx / BN;
                     st_shared(sb + sw128_offset(n, k * sizeof(E)), v[u]);
                 }
             }
@@ -498,14 +549,13 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
                 // groups of the tile are 1024 bytes apart.
                 const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
                 uint64_t db;
-                if constexpr (kKind == kF16 || !kTma) {
+                if constexpr (!T::kBNMajor || !kTma) {
                     // B staged K-major like A
                     db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
                 } else {
-                    // B (N-major, 32-byte swizzle atoms): one MMA covers 8 K-rows
-                    // (1 KB), read as two 4-row groups 512 B apart; 32-wide N
-                    // columns are 4 KB apart.
-                    db = ptx::smem_desc(sb + k * 1024, 4096, 512, ptx::kSw128A32);
+                    // B N-major: one MMA's K rows per step; boxes of 128
+                    // bytes of columns are kNBoxBytes apart
+                    db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
                 }
                 ptx::umma<kKind>(d_tmem, da, db, kTma ? T::kIdesc : T::kIdescKMajorB,
                                  (kb != sc.kb0 || k != 0) ? 1u : 0u);
@@ -536,10 +586,11 @@ template <int kKind>
 __device__ __forceinline__ void store_chunk(const Params &p, int64_t row, int64_t col,
                                             const uint32_t (&r)[32])
 {
+    using T = Traits<kKind>;
     if (row >= p.M) return;
     const float alpha = p.alpha, beta = p.beta;
-    if constexpr (kKind == kF16) {
-        __half *crow = reinterpret_cast<__half *>(p.C) + row * p.ldc;
+    if constexpr (T::kElem == 2) {
+        uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + row * p.ldc;
         if (p.vec_c && col + 31 < p.N) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -549,27 +600,24 @@ __device__ __forceinline__ void store_chunk(const Params &p, int64_t row, int64_
                 for (int e = 0; e < 8; ++e) v[e] = alpha * as_f(r[q * 8 + e]);
                 if (beta != 0.f) {
                     const uint4 old = *dst;
-                    const __half2 *h = reinterpret_cast<const __half2 *>(&old);
+                    const uint32_t *w = reinterpret_cast<const uint32_t *>(&old);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(h[e]);
+                        const float2 f = unpack2<T::kBF>(w[e]);
                         v[2 * e] = fmaf(beta, f.x, v[2 * e]);
                         v[2 * e + 1] = fmaf(beta, f.y, v[2 * e + 1]);
                     }
                 }
-                uint4 out;
-                __half2 *o = reinterpret_cast<__half2 *>(&out);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[e] = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
-                *dst = out;
+                *dst = make_uint4(pack2<T::kBF>(v[0], v[1]), pack2<T::kBF>(v[2], v[3]),
+                                  pack2<T::kBF>(v[4], v[5]), pack2<T::kBF>(v[6], v[7]));
             }
         } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 if (col + e < p.N) {
                     float v = alpha * as_f(r[e]);
-                    if (beta != 0.f) v = fmaf(beta, __half2float(crow[col + e]), v);
-                    crow[col + e] = __float2half_rn(v);
+                    if (beta != 0.f) v = fmaf(beta, load1<T::kBF>(crow + col + e), v);
+                    crow[col + e] = round1<T::kBF>(v);
                 }
             }
         }
@@ -621,7 +669,7 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + static_cast
 template <int kKind>
 constexpr int box_cols()
 {
-    return kKind == kF16 ? 64 : 32;
+    return Traits<kKind>::kElem == 2 ? 64 : 32;
 }
 
 // C_old for one row and one box of columns (masked, zeros outside C).
@@ -632,16 +680,17 @@ __device__ __forceinline__ void load_old(const Params &p, int64_t row, int64_t c
 #pragma unroll
     for (int e = 0; e < COLS; ++e) old[e] = 0.f;
     if (row >= p.M) return;
-    if constexpr (kKind == kF16) {
-        const __half *crow = reinterpret_cast<const __half *>(p.C) + row * p.ldc;
+    if constexpr (Traits<kKind>::kElem == 2) {
+        constexpr bool kBF = Traits<kKind>::kBF;
+        const uint16_t *crow = reinterpret_cast<const uint16_t *>(p.C) + row * p.ldc;
         if (p.vec_c && col + COLS - 1 < p.N) {
 #pragma unroll
             for (int q = 0; q < COLS / 8; ++q) {
                 const uint4 u = *reinterpret_cast<const uint4 *>(crow + col + q * 8);
-                const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+                const uint32_t *w = reinterpret_cast<const uint32_t *>(&u);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(h[e]);
+                    const float2 f = unpack2<kBF>(w[e]);
                     old[q * 8 + 2 * e] = f.x;
                     old[q * 8 + 2 * e + 1] = f.y;
                 }
@@ -649,7 +698,7 @@ __device__ __forceinline__ void load_old(const Params &p, int64_t row, int64_t c
         } else {
 #pragma unroll
             for (int e = 0; e < COLS; ++e)
-                if (col + e < p.N) old[e] = __half2float(crow[col + e]);
+                if (col + e < p.N) old[e] = load1<kBF>(crow + col + e);
         }
     } else {
         const float *crow = reinterpret_cast<const float *>(p.C) + row * p.ldc;
@@ -716,11 +765,10 @@ __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *t
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             uint4 q;
-            if constexpr (kKind == kF16) {
-                __half2 h[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[j * 8 + 2 * e], v[j * 8 + 2 * e + 1]);
-                q = *reinterpret_cast<uint4 *>(h);
+            if constexpr (Traits<kKind>::kElem == 2) {
+                constexpr bool kBF = Traits<kKind>::kBF;
+                q = make_uint4(pack2<kBF>(v[j * 8 + 0], v[j * 8 + 1]), pack2<kBF>(v[j * 8 + 2], v[j * 8 + 3]),
+                               pack2<kBF>(v[j * 8 + 4], v[j * 8 + 5]), pack2<kBF>(v[j * 8 + 6], v[j * 8 + 7]));
             } else {
                 q = make_uint4(__float_as_uint(v[j * 4 + 0]), __float_as_uint(v[j * 4 + 1]),
                                __float_as_uint(v[j * 4 + 2]), __float_as_uint(v[j * 4 + 3]));
@@ -1019,13 +1067,13 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
             const int32_t kc = static_cast<int32_t>(kb * T::BK);
             ptx::tma_load_2d_pair(sa, tmap_a, full, kc, static_cast<int32_t>(m0 + rank * 128));
             const int64_t nb = n0 + rank * 128;  // this CTA's half of B
-            if constexpr (kKind == kF16) {
+            if constexpr (!T::kBNMajor) {
                 ptx::tma_load_2d_pair(sb, tmap_b, full, kc, static_cast<int32_t>(nb));
             } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    ptx::tma_load_2d_pair(sb + c * 4096, tmap_b, full,
-                                          static_cast<int32_t>(nb + c * 32), kc);
+                for (int c = 0; c < 128 / T::kNBox; ++c)
+                    ptx::tma_load_2d_pair(sb + c * T::kNBoxBytes, tmap_b, full,
+                                          static_cast<int32_t>(nb + c * T::kNBox), kc);
             }
             issued |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -1074,10 +1122,10 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
             for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
                 const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
                 uint64_t db;
-                if constexpr (kKind == kF16)
+                if constexpr (!T::kBNMajor)
                     db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
                 else
-                    db = ptx::smem_desc(sb + k * 1024, 4096, 512, ptx::kSw128A32);
+                    db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
                 ptx::umma_pair<kKind>(d_tmem, da, db, pair_idesc<kKind>(), (kb | k) != 0 ? 1u : 0u);
             }
             ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), 0x3);
@@ -1413,17 +1461,25 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorM
     return true;
 }
 
-const char *splitk_name(int kind, int s)
+// Variant names ("umma_<kind>_<variant>"), built once per kind.
+template <int kKind>
+const char *variant_name(int variant, int split)
 {
-    static const char *f16[9] = {"", "", "umma_f16_tn_splitk2_128x256x64_tma",
-                                 "umma_f16_tn_splitk3_128x256x64_tma", "umma_f16_tn_splitk4_128x256x64_tma",
-                                 "umma_f16_tn_splitk5_128x256x64_tma", "umma_f16_tn_splitk6_128x256x64_tma",
-                                 "umma_f16_tn_splitk7_128x256x64_tma", "umma_f16_tn_splitk8_128x256x64_tma"};
-    static const char *tf32[9] = {"", "", "umma_tf32_splitk2_128x256x32_tma",
-                                  "umma_tf32_splitk3_128x256x32_tma", "umma_tf32_splitk4_128x256x32_tma",
-                                  "umma_tf32_splitk5_128x256x32_tma", "umma_tf32_splitk6_128x256x32_tma",
-                                  "umma_tf32_splitk7_128x256x32_tma", "umma_tf32_splitk8_128x256x32_tma"};
-    return kind == kF16 ? f16[s] : tf32[s];
+    static std::string names[12];  // 0 pair, 1 single TMA, 2 register / cp.async, 3+S split-K
+    static std::once_flag once;
+    std::call_once(once, [] {
+        using T = Traits<kKind>;
+        const char *kind = kKind == kF16 ? "f16_tn" : kKind == kTF32 ? "tf32" : kKind == kBF16 ? "bf16_tn"
+                         : kKind == kF16NN ? "f16_nn" : "bf16_nn";
+        const std::string bk = std::to_string(T::BK);
+        const std::string base = std::string("umma_") + kind;
+        names[0] = base + "_pair_256x256x" + bk + "_tma";
+        names[1] = base + "_128x256x" + bk + "_tma";
+        names[2] = base + "_128x256x" + bk + (kKind == kTF32 ? "_cpasync" : "_ldst");
+        for (int S = 2; S <= 8; ++S)
+            names[3 + S] = base + "_splitk" + std::to_string(S) + "_128x256x" + bk + "_tma";
+    });
+    return names[variant == 3 ? 3 + split : variant].c_str();
 }
 
 // TMA-capable operands: split-K for few tiles, CTA pairs for M > 128, else
@@ -1432,13 +1488,15 @@ const char *splitk_name(int kind, int s)
 template <int kKind>
 const char *dispatch_tma(const Params &p, const CUtensorMap &ma, const CUtensorMap &mb,
                          const CUtensorMap *mb_pair, const CUtensorMap &mc, cudaStream_t stream,
-                         const DeviceInfo &dev, const char *pair_name, const char *single_name)
+                         const DeviceInfo &dev)
 {
+    const char *pair_name = variant_name<kKind>(0, 0);
+    const char *single_name = variant_name<kKind>(1, 0);
     const int S = choose_splitk<kKind>(p, dev.sm_count);
     if (S > 1) {
         Params ps = p;
         ps.splitk = S;
-        if (launch_splitk<kKind>(ma, mb, mc, ps, stream)) return splitk_name(kKind, S);
+        if (launch_splitk<kKind>(ma, mb, mc, ps, stream)) return variant_name<kKind>(3, S);
     }
     if (mb_pair && p.M > BM) {
         Params pp = p;
@@ -1448,56 +1506,64 @@ const char *dispatch_tma(const Params &p, const CUtensorMap &ma, const CUtensorM
     return launch<kKind, true>(ma, mb, mc, p, stream, dev) ? single_name : nullptr;
 }
 
-}  // namespace
-
-const char *launch_umma_f16_tn(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
-                               int64_t lda, const uint16_t *B, int64_t ldb, float beta,
-                               uint16_t *C, int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
+template <int kKind>
+const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                        const void *B, int64_t ldb, float beta, void *C, int64_t ldc,
+                        cudaStream_t stream, const DeviceInfo &dev)
 {
-    Params p = make_params(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, Traits<kF16>::BK,
-                           aligned16(C) && (ldc % 8 == 0));
+    using T = Traits<kKind>;
+    constexpr int es = T::kElem;
+    const CUtensorMapDataType dt = T::kTf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : T::kBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    Params p = make_params(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, T::BK,
+                           aligned16(C) && (ldc * es) % 16 == 0);
     CUtensorMap mc{};
-    p.tma_store = (p.vec_c && make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, ldc * 2,
-                                       box_cols<kF16>(), 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    p.tma_store = (p.vec_c && make_map(&mc, dt, C, N, M, ldc * es, box_cols<kKind>(), 32,
+                                       CU_TENSOR_MAP_SWIZZLE_128B))
                       ? 1 : 0;
     // TMA needs 16-byte aligned bases and row pitches.
-    const bool tma = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
+    const bool tma = aligned16(A) && aligned16(B) && (lda * es) % 16 == 0 && (ldb * es) % 16 == 0;
     CUtensorMap ma{}, mb{}, mbp{};
-    if (tma &&
-        make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, Traits<kF16>::BK, BM,
-                 CU_TENSOR_MAP_SWIZZLE_128B) &&
-        make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2, Traits<kF16>::BK, BN,
-                 CU_TENSOR_MAP_SWIZZLE_128B)) {
-        const bool pair_map = make_map(&mbp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, ldb * 2,
-                                       Traits<kF16>::BK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-        return dispatch_tma<kF16>(p, ma, mb, pair_map ? &mbp : nullptr, mc, stream, dev,
-                                  "umma_f16_tn_pair_256x256x64_tma", "umma_f16_tn_128x256x64_tma");
+    if (tma && make_map(&ma, dt, A, K, M, lda * es, T::BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) {
+        bool ok_b, ok_pair;
+        if constexpr (T::kBNMajor) {
+            // B stored K x N: boxes of 128 bytes of columns x BK rows, shared
+            // by the single-CTA and pair kernels
+            ok_b = make_map(&mb, dt, B, N, K, ldb * es, T::kNBox, T::BK,
+                            T::kTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
+            mbp = mb;
+            ok_pair = ok_b;
+        } else {
+            // B stored N x K: BN-row boxes (single CTA), 128-row boxes (pair)
+            ok_b = make_map(&mb, dt, B, K, N, ldb * es, T::BK, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+            ok_pair = make_map(&mbp, dt, B, K, N, ldb * es, T::BK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        }
+        if (ok_b) return dispatch_tma<kKind>(p, ma, mb, ok_pair ? &mbp : nullptr, mc, stream, dev);
     }
-    return launch<kF16, false>(ma, mb, mc, p, stream, dev) ? "umma_f16_tn_128x256x64_ldst" : nullptr;
+    return launch<kKind, false>(ma, mb, mc, p, stream, dev) ? variant_name<kKind>(2, 0) : nullptr;
 }
 
-const char *launch_umma_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
-                             int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-                             int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
+}  // namespace
+
+const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+                        int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc,
+                        cudaStream_t stream, const DeviceInfo &dev)
 {
-    Params p = make_params(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, Traits<kTF32>::BK,
-                           aligned16(C) && (ldc % 4 == 0));
-    CUtensorMap mc{};
-    p.tma_store = (p.vec_c && make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, ldc * 4,
-                                       box_cols<kTF32>(), 32, CU_TENSOR_MAP_SWIZZLE_128B))
-                      ? 1 : 0;
-    const bool tma = aligned16(A) && aligned16(B) && (lda * 4) % 16 == 0 && (ldb * 4) % 16 == 0;
-    CUtensorMap ma{}, mb{};
-    if (tma &&
-        make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, Traits<kTF32>::BK, BM,
-                 CU_TENSOR_MAP_SWIZZLE_128B) &&
-        make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, N, K, ldb * 4, 32, Traits<kTF32>::BK,
-                 CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)) {
-        // TF32's B boxes are 32 x 32 for both kernels: one map serves both
-        return dispatch_tma<kTF32>(p, ma, mb, &mb, mc, stream, dev, "umma_tf32_pair_256x256x32_tma",
-                                   "umma_tf32_128x256x32_tma");
+    switch (kind) {
+    case kUmmaF16TN:
+        return launch_kind<kF16>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+    case kUmmaTF32NN:
+        return launch_kind<kTF32>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+    case kUmmaBF16TN:
+        return launch_kind<kBF16>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+    case kUmmaF16NN:
+        return launch_kind<kF16NN>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+    case kUmmaBF16NN:
+        return launch_kind<kBF16NN>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+    default:
+        return nullptr;
     }
-    return launch<kTF32, false>(ma, mb, mc, p, stream, dev) ? "umma_tf32_128x256x32_cpasync" : nullptr;
 }
 
 void umma_inject_stall(uint64_t wait_limit_ns)

@@ -36,7 +36,7 @@
  * Validation happens on the host before any launch; an invalid call writes
  *   nothing and launches nothing.  DGEMM_ERR_INVALID_ARG is returned for
  *   M, N or K < 0; a leading dimension smaller than its row length
- *   (lda < K; ldb < N for the NN calls, ldb < K for the TN call; ldc < N);
+ *   (lda < K; ldb < N for the NN calls, ldb < K for the TN calls; ldc < N);
  *   a NULL pointer for an operand that would be read or written.
  * DGEMM_ERR_UNSUPPORTED_DEVICE: the current device is not compute
  *   capability 10.3.
@@ -116,6 +116,36 @@ int gemm_tf32(int64_t M, int64_t N, int64_t K, float alpha,
 int gemm_f16_tn(int64_t M, int64_t N, int64_t K, float alpha,
                 const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
                 float beta, uint16_t *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * gemm_f16_nn -- HGEMM with every matrix row-major: C = alpha * A * B + beta * C.
+ *   A, lda  : device, IEEE binary16, M x K row-major.
+ *   B, ldb  : device, IEEE binary16, K x N row-major, (k, n) at B[k*ldb + n]
+ *             (ldb >= N).
+ *   C, ldc  : device, IEEE binary16, M x N row-major.
+ * Arithmetic, rounding and special cases as gemm_f16_tn.
+ * Source: "HGEMM SMEM Swizzle 代码学习", the kernel source's layout notes
+ * ("NN: A/B/C all row major", next to the TN layout it implements).
+ */
+int gemm_f16_nn(int64_t M, int64_t N, int64_t K, float alpha,
+                const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                float beta, uint16_t *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * gemm_bf16_tn / gemm_bf16_nn -- the same two layouts with bfloat16 A, B and
+ * C (raw 16-bit patterns: 1 sign, 8 exponent, 7 fraction bits): products
+ * accumulate in FP32 on the tensor cores; alpha*acc + beta*C_old is formed in
+ * FP32 and rounded once to bfloat16 (nearest even).  TN: B stored N x K
+ * (ldb >= K); NN: B stored K x N (ldb >= N).
+ * Source: "SGEMM CUDA代码学习", section "第 5 步" (BF16 among the tensor-core
+ * precisions, beside FP16 and TF32) with the layouts above.
+ */
+int gemm_bf16_tn(int64_t M, int64_t N, int64_t K, float alpha,
+                 const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                 float beta, uint16_t *C, int64_t ldc, cudaStream_t stream);
+int gemm_bf16_nn(int64_t M, int64_t N, int64_t K, float alpha,
+                 const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                 float beta, uint16_t *C, int64_t ldc, cudaStream_t stream);
 
 /* A static, NUL-terminated description of a dgemm_status value. */
 const char *dgemm_status_string(int status);

@@ -13,6 +13,9 @@ Sources (page title, section):
   * "SGEMM CUDA代码学习", "第 5 步" -- TF32 is 1+8+10 bits.
   * "Warp Specialization HGEMM", "6. B 的 RowMajor(K,N) 与 TN 布局" -- the TN
     layout: B is stored N x K and C = A * B^T.
+  * "HGEMM SMEM Swizzle 代码学习", the kernel source's layout notes -- NN: A, B,
+    C all row-major; TN: B stored N x K.
+  * "SGEMM CUDA代码学习", "第 5 步" -- BF16 among the tensor-core precisions.
 
 Acceptance, per element (the tolerance rule the method is judged by):
     |C_gpu - ref| <= tol * (|A||B|)_ij + tol * |beta * c_ij|
@@ -30,9 +33,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "dgemm_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-F32, TF32_NEAREST_AWAY, TF32_TRUNCATE, F16 = 0, 1, 2, 3
+F32, TF32_NEAREST_AWAY, TF32_TRUNCATE, F16, BF16 = 0, 1, 2, 3, 4
 _KIND = {"f32": F32, "tf32": TF32_NEAREST_AWAY, "tf32_rna": TF32_NEAREST_AWAY,
-         "tf32_rz": TF32_TRUNCATE, "f16": F16}
+         "tf32_rz": TF32_TRUNCATE, "f16": F16, "bf16": BF16}
 
 # Acceptance tolerances per path (relative to |A||B| and |beta*C|).
 def tol_f32(K: int) -> float:
@@ -41,6 +44,11 @@ def tol_f32(K: int) -> float:
 
 TOL_TF32 = 2e-3
 TOL_F16 = 1e-3
+# BF16 (no tolerance is fixed for it): bfloat16 keeps 8 significant bits, so
+# the single rounding of the result costs up to half an ulp, 2^-8 of |result|
+# <= 2^-8 * (|alpha| |A||B| + |beta c|) -- at most 1.5 * 2^-8 = 5.9e-3 of the
+# bound's terms for |alpha| <= 1.5; FP32 accumulation adds ~K * 2^-24.
+TOL_BF16 = 8e-3
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +72,8 @@ def load_library(path: str):
     i64, dbl, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
     lib.oracle_f16_value.restype = dbl
     lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_value.restype = dbl
+    lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
     lib.oracle_tf32_value.restype = dbl
     lib.oracle_tf32_value.argtypes = [ctypes.c_float, ctypes.c_int]
     lib.oracle_widen.restype = None
@@ -91,6 +101,11 @@ def f16_value(bits: int) -> float:
     return _load().oracle_f16_value(bits)
 
 
+def bf16_value(bits: int) -> float:
+    """The value of one bfloat16 bit pattern."""
+    return _load().oracle_bf16_value(bits)
+
+
 def tf32_value(x: float, mode: str = "tf32_rna") -> float:
     """One float reduced to TF32 (mode 'tf32_rna' or 'tf32_rz')."""
     return _load().oracle_tf32_value(x, _KIND[mode])
@@ -103,7 +118,7 @@ def widen(kind: str, m: np.ndarray, trans: bool = False) -> np.ndarray:
     f16) whose rows may be padded (a row stride above its width).  With
     ``trans`` the logical matrix is m^T (the TN store of B)."""
     code = _KIND[kind]
-    if code == F16:
+    if code in (F16, BF16):
         if m.dtype == np.float16:
             m = m.view(np.uint16)
         assert m.dtype == np.uint16
@@ -168,10 +183,11 @@ def reference(kind: str, A: np.ndarray, B: np.ndarray, C, alpha: float, beta: fl
               *, tn: bool = False, **select):
     """Widen the stored operands for path ``kind`` and evaluate the product.
 
-    kind: 'f32', 'tf32_rna', 'tf32_rz' or 'f16'.  For 'f16', ``tn`` is the
-    layout flag (B stored N x K).  C is widened as stored (f32, or f16 for the
-    f16 path) and ignored when beta == 0."""
-    ck = "f16" if kind == "f16" else "f32"
+    kind: 'f32', 'tf32_rna', 'tf32_rz', 'f16' or 'bf16' (16-bit operands as
+    uint16 bit patterns or float16).  ``tn`` is the layout flag (B stored
+    N x K).  C is widened as stored (f32, or the 16-bit kind) and ignored when
+    beta == 0."""
+    ck = kind if kind in ("f16", "bf16") else "f32"
     A64 = widen(kind, A)
     B64 = widen(kind, B, trans=tn)
     C64 = widen(ck, C) if beta != 0.0 else None

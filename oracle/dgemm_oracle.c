@@ -19,7 +19,8 @@
  *   - TF32 operands: each float first reduced to TF32 (1 sign, 8 exponent,
  *     10 mantissa bits), round-to-nearest-ties-away or truncation;
  *   - FP16 operands: the IEEE binary16 values;
- *   - TN layout: b[k][j] is read from the store at B[j*ldb + k].
+ *   - BF16 operands: the bfloat16 values (the top half of a float);
+ *   - TN layout: b[k][j] is read from the store at B[j*ldb + k]; NN: B[k*ldb + j].
  * When beta == 0 the C term is dropped (C is never read), and when
  * alpha == 0 or K == 0 the sum is skipped (A and B are never read).
  *
@@ -50,6 +51,7 @@
 #define ORACLE_OPERAND_TF32_NEAREST_AWAY 1
 #define ORACLE_OPERAND_TF32_TRUNCATE 2
 #define ORACLE_OPERAND_F16 3
+#define ORACLE_OPERAND_BF16 4
 
 /* ------------------------------------------------------------------ */
 /* Operand value definitions                                           */
@@ -70,6 +72,24 @@ double oracle_f16_value(uint16_t h)
         v = (f == 0) ? INFINITY : NAN;
     else
         v = ldexp(1024.0 + (double)f, e - 25); /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 -> double, from the format: 1 sign bit, 8 exponent bits (bias
+ * 127, as for float), 7 fraction bits; exponent 0 encodes subnormals
+ * f * 2^-133, exponent 255 infinities (f == 0) and NaNs. */
+double oracle_bf16_value(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 255;
+    int f = h & 127;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);
+    else if (e == 255)
+        v = (f == 0) ? INFINITY : NAN;
+    else
+        v = ldexp(128.0 + (double)f, e - 134); /* (1 + f/128) * 2^(e-127) */
     return sign ? -v : v;
 }
 
@@ -112,6 +132,8 @@ void oracle_widen(int kind, const void *src, int64_t rows, int64_t cols,
             double v;
             if (kind == ORACLE_OPERAND_F16)
                 v = oracle_f16_value(((const uint16_t *)src)[at]);
+            else if (kind == ORACLE_OPERAND_BF16)
+                v = oracle_bf16_value(((const uint16_t *)src)[at]);
             else if (kind == ORACLE_OPERAND_F32)
                 v = (double)((const float *)src)[at];
             else

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("gemm_f32", "gemm_tf32", "gemm_f16_tn", "dgemm_status_string"):
+    for n in ENTRY + ["dgemm_status_string", "dgemm_device_status"]:
         assert n in names
 
 
@@ -56,7 +56,7 @@ def test_status_strings(L):
     assert "unknown" in dg.status_string(99)
 
 
-ENTRY = ["gemm_f32", "gemm_tf32", "gemm_f16_tn"]
+ENTRY = ["gemm_f32", "gemm_tf32", "gemm_f16_tn", "gemm_f16_nn", "gemm_bf16_tn", "gemm_bf16_nn"]
 P = 0x1000  # a non-null dummy pointer value (never dereferenced: validation fails first)
 
 
@@ -87,7 +87,7 @@ def test_empty_problem_returns_ok_without_device(L, name):
 def test_tn_ldb_rule(L, name):
     # TN: B is N x K, so ldb >= K is the rule (K=16 > N=8 here)
     st = getattr(L, name)(8, 8, 16, 1.0, P, 16, P, 8, 0.0, P, 8, None)
-    if name == "gemm_f16_tn":
+    if name.endswith("_tn"):
         assert st == 1
     else:
         assert st != 1  # ldb = N = 8 is valid for the NN calls

@@ -50,3 +50,17 @@ def test_config(name, path, full):
         worst = parity.sampled_check(path, dC, A, B, C, w.alpha, w.beta)
     assert worst <= 1.0, worst
     assert torch.isfinite(dC).all()
+
+
+# The layout / type variants at a full square size: FP16 NN and BF16 TN / NN,
+# seeded uniform operands (rounded to the 16-bit type), checked in full.
+@pytest.mark.parametrize("path", ["f16_nn", "bf16_tn", "bf16_nn"])
+def test_variant_4096_cube_full(path):
+    import dense_gemm_09_gb300 as dg
+    A, B, C = parity.host_operands(path, 4096, 4096, 4096, seed=17)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    parity.fn(path)(dA, dB, dC, 1.5, -0.25)
+    torch.cuda.synchronize()
+    assert dg.device_status() == dg.OK
+    assert "_pair_" in dg.last_kernel()
+    assert parity.worst_ratio(path, dC.cpu(), A, B, C, 1.5, -0.25) <= 1.0

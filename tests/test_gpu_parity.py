@@ -40,6 +40,10 @@ SHAPES = {
                (300, 520, 1000), (1, 300, 704), (700, 1, 304), (64, 1000, 8),
                (1, 1, 1), (5, 7, 3), (17, 9, 33), (129, 127, 17), (255, 257, 301)],
 }
+# The other 16-bit paths (FP16 NN, BF16 TN / NN) take the FP16 TN shape list:
+# NN pitches of N elements are TMA-capable when N is a multiple of 8.
+for _p in ("f16_nn", "bf16_tn", "bf16_nn"):
+    SHAPES[_p] = SHAPES["f16_tn"]
 
 
 @pytest.mark.parametrize("path,shape", [(p, s) for p in parity.PATHS for s in SHAPES[p]])
@@ -61,15 +65,19 @@ def test_beta_zero_alpha_one(path):
 @pytest.mark.parametrize("path,shape", [
     ("f32", (64, 72, 300)), ("f32", (129, 257, 1000)),
     ("tf32", (64, 72, 300)), ("tf32", (129, 260, 1000)),
-    ("f16_tn", (64, 72, 304)), ("f16_tn", (129, 257, 1024))])
+    ("f16_tn", (64, 72, 304)), ("f16_tn", (129, 257, 1024)),
+    ("f16_nn", (64, 72, 304)), ("f16_nn", (129, 264, 1024)),
+    # bfloat16 holds integers exactly up to 256: |sum| <= K + 1 must stay below
+    ("bf16_tn", (64, 72, 200)), ("bf16_tn", (129, 257, 248)),
+    ("bf16_nn", (64, 72, 200)), ("bf16_nn", (129, 264, 248))])
 def test_small_integers_bit_exact(path, shape):
     # every partial sum is an integer below 2^24: any summation order is exact
     M, N, K = shape
     A, B, C = parity.host_operands(path, M, N, K, seed=11, dist="int")
-    beta = 2.0 if path != "f16_tn" else 1.0
+    beta = 2.0 if path in ("f32", "tf32") else 1.0
     got, _, _ = parity.run(path, A, B, C, 1.0, beta)
     ref, _ = parity.reference(path, A, B, C, 1.0, beta)
-    assert np.array_equal(got.numpy().astype(np.float64), ref)
+    assert np.array_equal(got.double().numpy(), ref)
 
 
 @pytest.mark.parametrize("path", parity.PATHS)
@@ -77,19 +85,19 @@ def test_identity_and_permutation_exact(path):
     M = 136
     N = 264
     g = si.generator(5)
-    dt = torch.float16 if path == "f16_tn" else torch.float32
+    dt = parity.dtype(path)
     perm = torch.randperm(M, generator=g)
     P = torch.zeros((M, M), dtype=dt)
     P[torch.arange(M), perm] = 1
     Bl = si.uniform((M, N), g).to(dt)          # logical B (K x N)
-    B = Bl.T.contiguous() if path == "f16_tn" else Bl
+    B = Bl.T.contiguous() if parity.is_tn(path) else Bl
     C = torch.zeros((M, N), dtype=dt)
     got, _, _ = parity.run(path, P, B, C, 1.0, 0.0)
     want = Bl[perm]
     if path == "tf32":
         # the product reads B through TF32: compare with the oracle's exact values
         ref, _ = parity.reference(path, P, B, C, 1.0, 0.0)
-        assert np.array_equal(got.numpy().astype(np.float64), ref)
+        assert np.array_equal(got.double().numpy(), ref)
     else:
         assert torch.equal(got, want)
 
@@ -120,7 +128,7 @@ def test_k_zero_scales_c(path):
     M, N = 33, 40
     _, _, C = parity.host_operands(path, M, N, 8, seed=6)
     A = torch.zeros((M, 0), dtype=C.dtype)
-    B = torch.zeros((0, N) if path != "f16_tn" else (N, 0), dtype=C.dtype)
+    B = torch.zeros((N, 0) if parity.is_tn(path) else (0, N), dtype=C.dtype)
     got, _, _ = parity.run(path, A, B, C, 1.0, -2.0)
     assert torch.equal(got, (C.double() * -2.0).to(C.dtype))
     got, _, _ = parity.run(path, A, B, C, 1.0, 0.0)
@@ -129,12 +137,11 @@ def test_k_zero_scales_c(path):
 
 @pytest.mark.parametrize("path", parity.PATHS)
 def test_empty_m_or_n_is_a_no_op(path):
-    import dense_gemm_09_gb300 as dg
-    dt = torch.float16 if path == "f16_tn" else torch.float32
-    fn = {"f32": dg.gemm_f32, "tf32": dg.gemm_tf32, "f16_tn": dg.gemm_f16_tn}[path]
+    dt = parity.dtype(path)
+    fn = parity.fn(path)
     for M, N in ((0, 16), (16, 0)):
         A = torch.ones((M, 8), dtype=dt, device="cuda")
-        B = torch.ones((8, N) if path != "f16_tn" else (N, 8), dtype=dt, device="cuda")
+        B = torch.ones((N, 8) if parity.is_tn(path) else (8, N), dtype=dt, device="cuda")
         C = torch.ones((M, N), dtype=dt, device="cuda")
         fn(A, B, C, 1.0, 1.0)
     torch.cuda.synchronize()
@@ -203,7 +210,7 @@ def test_tf32_operand_rounding_is_truncation():
     assert np.array_equal(got.numpy().astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
+@pytest.mark.parametrize("path", parity.TC_PATHS)
 @pytest.mark.parametrize("shape,pad,offset", [
     ((131, 133, 137), (1, 3, 1), (1, 2, 3)),      # odd pitches, misaligned bases
     ((300, 520, 256), (1, 0, 0), (0, 0, 0)),      # only A's pitch is odd
@@ -216,18 +223,18 @@ def test_tensor_paths_register_producer(path, shape, pad, offset):
     M, N, K = shape
     A, B, C = parity.host_operands(path, M, N, K, seed=M + N + K)
     got, _, _ = parity.run(path, A, B, C, 1.5, -0.25, pad=pad, offset=offset)
-    # FP16: loads through registers; TF32: 4-byte cp.async copies
-    assert dg.last_kernel().endswith("_ldst" if path == "f16_tn" else "_cpasync")
+    # 16-bit: loads through registers; TF32: 4-byte cp.async copies
+    assert dg.last_kernel().endswith("_cpasync" if path == "tf32" else "_ldst")
     assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
 
 
-@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
+@pytest.mark.parametrize("path", parity.TC_PATHS)
 def test_register_producer_integers_bit_exact(path):
-    M, N, K = 257, 300, 259
+    M, N, K = 257, 300, (203 if path.startswith("bf16") else 259)
     A, B, C = parity.host_operands(path, M, N, K, seed=21, dist="int")
     got, _, _ = parity.run(path, A, B, C, 1.0, 1.0)
     ref, _ = parity.reference(path, A, B, C, 1.0, 1.0)
-    assert np.array_equal(got.numpy().astype(np.float64), ref)
+    assert np.array_equal(got.double().numpy(), ref)
 
 
 @pytest.mark.parametrize("path", parity.PATHS)
@@ -235,7 +242,7 @@ def test_kernel_variant_names(path):
     import dense_gemm_09_gb300 as dg
     A, B, C = parity.host_operands(path, 256, 256, 256, seed=1)
     parity.run(path, A, B, C, 1.0, 0.0)
-    want = {"f32": "sgemm_simt", "tf32": "umma_tf32", "f16_tn": "umma_f16_tn"}[path]
+    want = "sgemm_simt" if path == "f32" else "umma_" + path
     assert dg.last_kernel().startswith(want)
     if path != "f32":
         # M > 128 and 16-byte pitches: the CTA-pair kernel
@@ -246,7 +253,7 @@ def test_kernel_variant_names(path):
         assert parity.worst_ratio(path, got, A, B, C, 1.0, 0.0) <= 1.0
 
 
-@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
+@pytest.mark.parametrize("path", parity.TC_PATHS)
 @pytest.mark.parametrize("M", [129, 200, 255, 256, 257, 383, 511, 640])
 def test_pair_kernel_m_tails(path, M):
     # the pair tile is 256 rows: the odd CTA's rows run past M in these cases
@@ -265,6 +272,9 @@ SPLITK_CASES = [
     ("f16_tn", (127, 2048, 1000)),   # K tail inside the last range
     ("tf32", (100, 520, 1000)),      # K tail, S = 8
     ("tf32", (256, 256, 2048)),
+    ("f16_nn", (100, 1000, 2048)),
+    ("bf16_tn", (127, 2048, 1000)),
+    ("bf16_nn", (300, 512, 4096)),
 ]
 
 
@@ -278,7 +288,7 @@ def test_splitk_kernel(path, shape):
     assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
 
 
-@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
+@pytest.mark.parametrize("path", ["tf32", "f16_tn", "f16_nn"])
 def test_splitk_integers_bit_exact(path):
     import dense_gemm_09_gb300 as dg
     M, N, K = 120, 600, 2048
@@ -286,7 +296,7 @@ def test_splitk_integers_bit_exact(path):
     got, _, _ = parity.run(path, A, B, C, 1.0, 1.0)
     assert "_splitk" in dg.last_kernel()
     ref, _ = parity.reference(path, A, B, C, 1.0, 1.0)
-    assert np.array_equal(got.numpy().astype(np.float64), ref)
+    assert np.array_equal(got.double().numpy(), ref)
 
 
 def test_splitk_is_deterministic():

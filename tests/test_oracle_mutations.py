@@ -32,6 +32,9 @@ MUTATIONS = {
     "tf32_no_subnormal_floor": ("if (e < -126)\n        e = -126;", "if (e < -160)\n        e = -160;"),
     "f16_bias_off_by_one": ("v = ldexp(1024.0 + (double)f, e - 25);", "v = ldexp(1024.0 + (double)f, e - 24);"),
     "f16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "bf16_bias_off_by_one": ("v = ldexp(128.0 + (double)f, e - 134);", "v = ldexp(128.0 + (double)f, e - 133);"),
+    "bf16_decoded_as_f16": ("v = oracle_bf16_value(((const uint16_t *)src)[at]);",
+                            "v = oracle_f16_value(((const uint16_t *)src)[at]);"),
     "entry_uses_wrong_b_index": ("double b = p->B[k * N + j];", "double b = p->B[j * N + k];"),
     "beta_scales_the_sum_too": ("v += p->beta * p->C[i * N + j];\n        ref[j] = v;",
                                 "v = p->beta * (v + p->C[i * N + j]);\n        ref[j] = v;"),
@@ -41,6 +44,8 @@ MUTATIONS = {
 
 PIN_FUNCS = [
     ("test_hand_products", True), ("test_tf32_fixture", True), ("test_f16_fixture", True),
+    ("test_bf16_fixture", True), ("test_bf16_all_patterns_match_torch", False),
+    ("test_bf16_nn_and_tn_products_exact", False),
     ("test_f16_all_patterns_match_numpy", False),
     ("test_exact_integer_products", "kinds"), ("test_identity_and_permutation", "sizes"),
     ("test_rank_one_known_sums", False), ("test_alpha_zero_never_reads_operands", False),

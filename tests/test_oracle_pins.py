@@ -79,6 +79,41 @@ def test_f16_fixture(golden_dir):
             assert v == want and np.signbit(v) == np.signbit(want), e
 
 
+def test_bf16_fixture(golden_dir):
+    g = _golden(golden_dir, "operand_values.json")
+    for e in g["bf16"]:
+        v = oracle.bf16_value(int(e["bits"], 16))
+        want = _hexf(e["value"])
+        if np.isnan(want):
+            assert np.isnan(v)
+        else:
+            assert v == want and np.signbit(v) == np.signbit(want), e
+
+
+def test_bf16_all_patterns_match_torch():
+    # every one of the 65536 bfloat16 patterns against torch's own decoder
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(256, 256)
+    mine = oracle.widen("bf16", bits)
+    theirs = torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).double().numpy()
+    same = (mine == theirs) | (np.isnan(mine) & np.isnan(theirs))
+    assert same.all()
+
+
+def test_bf16_nn_and_tn_products_exact():
+    # small integers are exact in bfloat16; NN reads B as K x N, TN as N x K
+    g = si.generator(13)
+    M, N, K = 9, 11, 40
+    A = si.small_integers((M, K), g, dtype=torch.bfloat16)
+    B = si.small_integers((K, N), g, dtype=torch.bfloat16)
+    C = si.small_integers((M, N), g, dtype=torch.bfloat16)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ref_nn, _ = oracle.reference("bf16", bits(A), bits(B), bits(C), 2.0, -1.0, tn=False)
+    ref_tn, _ = oracle.reference("bf16", bits(A), bits(B.T), bits(C), 2.0, -1.0, tn=True)
+    Ai, Bi, Ci = (t.to(torch.int64).numpy() for t in (A, B, C))
+    want = (2 * (Ai @ Bi) - Ci).astype(np.float64)
+    assert np.array_equal(ref_nn, want) and np.array_equal(ref_tn, want)
+
+
 def test_f16_all_patterns_match_numpy():
     # every one of the 65536 binary16 patterns against numpy's own decoder
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(256, 256)
