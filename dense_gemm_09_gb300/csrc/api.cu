@@ -87,7 +87,7 @@ extern "C" int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const floa
     DeviceInfo dev;
     if ((st = check_device(dev)) != DGEMM_OK) return st;
     if (K == 0 || alpha == 0.f) return finish(launch_scale_f32(M, N, beta, C, ldc, stream));
-    return finish(launch_sgemm_simt(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream));
+    return finish(launch_sgemm_simt(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev));
 }
 
 extern "C" int gemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,

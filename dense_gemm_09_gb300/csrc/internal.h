@@ -16,9 +16,6 @@ inline bool aligned16(const void *p)
 // Each launcher enqueues its kernel(s) on `stream` and returns the name of
 // the variant it chose.  Arguments have been validated by the caller.
 
-const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
-                              int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-                              int64_t ldc, cudaStream_t stream);
 
 // C = beta * C (beta == 0: C = 0), for K == 0 or alpha == 0.
 const char *launch_scale_f32(int64_t M, int64_t N, float beta, float *C, int64_t ldc,
@@ -33,6 +30,12 @@ struct DeviceInfo {
     int sm_count = 0;
     int max_smem_optin = 0;
 };
+
+// FP32 SIMT path: the one-tile-per-CTA kernel, plus a split-K launch in
+// clusters for the last partial wave (or for the whole of a small problem).
+const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                              int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                              int64_t ldc, cudaStream_t stream, const DeviceInfo &dev);
 
 // Tensor-core paths: operand kinds (TN = B stored N x K, NN = B stored K x N).
 enum UmmaKind { kUmmaF16TN = 0, kUmmaTF32NN = 1, kUmmaBF16TN = 2, kUmmaF16NN = 3, kUmmaBF16NN = 4 };

@@ -240,6 +240,14 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
+// Number of CTAs in this CTA's cluster.
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
 // All threads of all CTAs in the cluster (release / acquire).
 __device__ __forceinline__ void cluster_sync()
 {
@@ -267,6 +275,25 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
 __device__ __forceinline__ void st_shared_cluster_f32(uint32_t cluster_addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
+// 16-byte store to the shared memory of a cluster CTA.
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, float4 v)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// 16-byte load from this CTA's shared memory.
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr)

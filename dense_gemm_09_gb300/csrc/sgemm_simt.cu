@@ -24,11 +24,24 @@
 //     k order.
 //   * Epilogue: alpha * acc + beta * C_old, C not read when beta == 0,
 //     16-byte stores where aligned.
+//   * Problems too small to fill the GPU (fewer tiles than resident CTAs, 2
+//     per SM) run split-K in clusters of S CTAs that each sum one contiguous
+//     range of K slices; the partial sums meet in distributed shared memory
+//     and are added in rank order, so the result does not depend on timing.
+//     This is the split-K that "如何优化一个 CUDA Matmul Kernel ... Worklog",
+//     section "Kernel 10: Warptiling", finds the vendor library using at
+//     size 256 (a matmul kernel, then a reduction); here the reduction
+//     happens inside the cluster, with no extra memory and no second kernel.
+//     (Splitting only the last partial wave of a large problem was measured
+//     and lost: as a second launch it waits for the first launch's slowest
+//     CTAs, and as one cluster launch the whole grid ran ~5 % slower.)
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dgemm {
 namespace {
@@ -146,11 +159,100 @@ __device__ __forceinline__ void epilogue_store(float *__restrict__ C, int64_t ld
     }
 }
 
-template <bool kVec>
+// ---- split-K across a cluster (the last partial wave, and small problems)
+//
+// The S CTAs of a cluster (S in {2, 3, 4, 5, 8}) share one tile; rank r sums
+// K slices [r*kt/S, (r+1)*kt/S).  Row i (0..7) of each thread's eight rows
+// belongs to rank i mod S.  Every rank stores the rows it does not own into
+// the owner's stage ring (idle by then) with remote 16-byte stores; after a
+// cluster barrier each owner adds the S partials in rank order 0..S-1 and
+// runs the ordinary epilogue on its rows.  Receive layout, in float4 units:
+// [sender slot among the other S-1 ranks][row index i/S][half h][thread],
+// so a warp's stores and loads are 512 contiguous bytes.
+constexpr int kSplitChoices[] = {8, 5, 4, 3, 2};
+
+__host__ __device__ constexpr uint32_t split_recv_bytes(uint32_t S)
+{
+    return (S - 1) * ((8 + S - 1) / S) * 2 * THREADS * 16;
+}
+static_assert(split_recv_bytes(2) <= uint32_t(SMEM_BYTES) && split_recv_bytes(3) <= uint32_t(SMEM_BYTES) &&
+                  split_recv_bytes(4) <= uint32_t(SMEM_BYTES) && split_recv_bytes(5) <= uint32_t(SMEM_BYTES) &&
+                  split_recv_bytes(8) <= uint32_t(SMEM_BYTES),
+              "split-K partials must fit in the stage ring");
+
+__device__ __forceinline__ uint32_t split_recv_offset(uint32_t slot, uint32_t il, uint32_t h,
+                                                      uint32_t S, int tid)
+{
+    const uint32_t il_max = (8 + S - 1) / S;
+    return (((slot * il_max + il) * 2 + h) * THREADS + static_cast<uint32_t>(tid)) * 16;
+}
+
+__device__ __forceinline__ void split_reduce_store(const float2 (&acc)[8][4], uint32_t smem0,
+                                                   uint32_t S, uint32_t rank, int tid,
+                                                   float *__restrict__ C, int64_t ldc, int64_t M,
+                                                   int64_t N, int64_t m0, int64_t n0, int ty,
+                                                   int tx, float alpha, float beta, bool vec_c)
+{
+    ptx::cluster_sync();  // every CTA of the cluster is done with its stage ring
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t owner = static_cast<uint32_t>(i) % S;
+        if (owner == rank) continue;
+        const uint32_t slot = rank < owner ? rank : rank - 1;
+        const uint32_t off = split_recv_offset(slot, static_cast<uint32_t>(i) / S, 0, S, tid);
+        const uint32_t dst = ptx::mapa(smem0 + off, owner);
+        ptx::st_shared_cluster_v4(dst, make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y));
+        ptx::st_shared_cluster_v4(dst + THREADS * 16,
+                                  make_float4(acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y));
+    }
+    ptx::cluster_sync();  // the partials have landed in their owners
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (static_cast<uint32_t>(i) % S != rank) continue;
+        float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
+        for (uint32_t q = 0; q < S; ++q) {
+            float4 l, h;
+            if (q == rank) {
+                l = make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
+                h = make_float4(acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y);
+            } else {
+                const uint32_t slot = q < rank ? q : q - 1;
+                const uint32_t off = split_recv_offset(slot, static_cast<uint32_t>(i) / S, 0, S, tid);
+                l = ptx::ld_shared_v4f(smem0 + off);
+                h = ptx::ld_shared_v4f(smem0 + off + THREADS * 16);
+            }
+            lo[0] += l.x; lo[1] += l.y; lo[2] += l.z; lo[3] += l.w;
+            hi[0] += h.x; hi[1] += h.y; hi[2] += h.z; hi[3] += h.w;
+        }
+        const int64_t gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+        epilogue_store(C, ldc, M, N, gm, n0 + tx * 4, lo, alpha, beta, vec_c);
+        epilogue_store(C, ldc, M, N, gm, n0 + 64 + tx * 4, hi, alpha, beta, vec_c);
+    }
+}
+
+// Launch modes.
+//   kPlain : one CTA per tile, tile tile0 + blockIdx.x.
+//   kSplit : clusters of S; cluster c splits tile tile0 + c over K.
+enum SimtMode { kPlain = 0, kSplit = 1 };
+
+// This CTA's share of its tile: S ranks split the tile's K slices (S = 1:
+// the whole tile); rank is the CTA's place among them.
+template <int kMode>
+__device__ __forceinline__ void split_role(uint32_t &S, uint32_t &rank)
+{
+    S = 1;
+    rank = 0;
+    if constexpr (kMode == kSplit) {
+        S = ptx::cluster_nctarank();
+        rank = ptx::cluster_ctarank();
+    }
+}
+
+template <bool kVec, int kMode>
 __global__ void __launch_bounds__(THREADS, 2)
     sgemm_simt_kernel(int64_t M, int64_t N, int64_t K, float alpha, const float *__restrict__ A,
                       int64_t lda, const float *__restrict__ B, int64_t ldb, float beta,
-                      float *__restrict__ C, int64_t ldc, bool vec_c)
+                      float *__restrict__ C, int64_t ldc, int64_t tile0, bool vec_c)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SimtStage *stages = reinterpret_cast<SimtStage *>(smem_raw);
@@ -165,10 +267,12 @@ __global__ void __launch_bounds__(THREADS, 2)
     // Grouped rasterisation of a 1-D grid: runs of kGroupM consecutive blocks
     // walk down M inside one N column, so blocks resident together share B
     // columns and a short band of A rows in L2.
+    uint32_t S, rank;
+    split_role<kMode>(S, rank);
+    const int64_t b = tile0 + blockIdx.x / S;
     int64_t m0, n0;
     {
         const int64_t tiles_m = (M + BM - 1) / BM;
-        const int64_t b = blockIdx.x;
         const int64_t per_group = static_cast<int64_t>(kGroupM) * ((N + BN - 1) / BN);
         const int64_t g = b / per_group, r = b % per_group;
         const int64_t gm = tiles_m - g * kGroupM < kGroupM ? tiles_m - g * kGroupM : kGroupM;
@@ -183,19 +287,24 @@ __global__ void __launch_bounds__(THREADS, 2)
         for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
     const int64_t kt_count = (K + BK - 1) / BK;
+    // (the host splits only when kt_count < 2^28, so 32-bit products suffice)
+    constexpr bool kMaySplit = kMode != kPlain;
+    const int64_t kt0 = kMaySplit ? static_cast<int64_t>(rank * static_cast<uint32_t>(kt_count) / S) : 0;
+    const int64_t kt1 =
+        kMaySplit ? static_cast<int64_t>((rank + 1) * static_cast<uint32_t>(kt_count) / S) : kt_count;
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < kt_count)
-            load_slice<kVec>(smem0 + s * sizeof(SimtStage), A, lda, B, ldb, M, N, K, m0, n0, s, warp,
-                             lane);
+        if (kt0 + s < kt1)
+            load_slice<kVec>(smem0 + s * sizeof(SimtStage), A, lda, B, ldb, M, N, K, m0, n0, kt0 + s,
+                             warp, lane);
         cp_async_commit();
     }
 
     int read_stage = 0, write_stage = STAGES - 1;
-    for (int64_t kt = 0; kt < kt_count; ++kt) {
+    for (int64_t kt = kt0; kt < kt1; ++kt) {
         cp_async_wait<STAGES - 2>();  // slice kt has landed (this thread's copies)
         __syncthreads();              // ... everyone's; and slice kt-1 is consumed
-        if (kt + STAGES - 1 < kt_count)
+        if (kt + STAGES - 1 < kt1)
             load_slice<kVec>(smem0 + static_cast<uint32_t>(write_stage) * sizeof(SimtStage), A, lda,
                              B, ldb, M, N, K, m0, n0, kt + STAGES - 1, warp, lane);
         cp_async_commit();
@@ -221,43 +330,160 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     cp_async_wait<0>();
 
+    if constexpr (kMaySplit) {
+        // S and rank are read again here rather than kept live through the loop
+        split_role<kMode>(S, rank);
+        split_reduce_store(acc, smem0, S, rank, tid, C, ldc, M, N, m0, n0, ty, tx, alpha, beta, vec_c);
+    } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int64_t gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
-        const float lo[4] = {acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y};
-        const float hi[4] = {acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y};
-        epilogue_store(C, ldc, M, N, gm, n0 + tx * 4, lo, alpha, beta, vec_c);
-        epilogue_store(C, ldc, M, N, gm, n0 + 64 + tx * 4, hi, alpha, beta, vec_c);
+        for (int i = 0; i < 8; ++i) {
+            const int64_t gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+            const float lo[4] = {acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y};
+            const float hi[4] = {acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y};
+            epilogue_store(C, ldc, M, N, gm, n0 + tx * 4, lo, alpha, beta, vec_c);
+            epilogue_store(C, ldc, M, N, gm, n0 + 64 + tx * 4, hi, alpha, beta, vec_c);
+        }
     }
 }
 
+// Occupancy facts of one kernel variant on one device, computed once.
+struct SimtOccupancy {
+    bool ready = false;
+    int blocks_per_sm = 0;      // resident CTAs per SM of the one-tile-per-CTA kernel
+    int clusters[9] = {};       // co-resident clusters of the split kernel, by size
+};
+
 template <bool kVec>
-void launch_kernel(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
-                   const float *B, int64_t ldb, float beta, float *C, int64_t ldc, bool vec_c,
-                   cudaStream_t stream)
+const SimtOccupancy &occupancy(int device)
 {
-    cudaFuncSetAttribute(sgemm_simt_kernel<kVec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr int kMaxDevices = 64;
+    static SimtOccupancy table[kMaxDevices];
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    SimtOccupancy &o = table[device >= 0 && device < kMaxDevices ? device : 0];
+    if (o.ready) return o;
+    cudaFuncSetAttribute(sgemm_simt_kernel<kVec, kPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          SMEM_BYTES);
-    const int64_t blocks = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    sgemm_simt_kernel<kVec><<<static_cast<unsigned>(blocks), THREADS, SMEM_BYTES, stream>>>(
-        M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, vec_c);
+    cudaFuncSetAttribute(sgemm_simt_kernel<kVec, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         SMEM_BYTES);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o.blocks_per_sm, sgemm_simt_kernel<kVec, kPlain>,
+                                                      THREADS, SMEM_BYTES) != cudaSuccess)
+        o.blocks_per_sm = 1;
+    for (int S : kSplitChoices) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(S));
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, sgemm_simt_kernel<kVec, kSplit>, &cfg) != cudaSuccess) n = 0;
+        o.clusters[S] = n;
+    }
+    cudaGetLastError();  // a refused query leaves no sticky error behind
+    o.ready = true;
+    return o;
+}
+
+// How one call is launched.  With W resident CTAs (2 per SM): fewer tiles
+// than W take one kSplit launch in clusters of the largest S in
+// {8, 5, 4, 3, 2} with tiles * S <= W, at least two K slices per rank and
+// every cluster resident at once; anything else one kPlain launch.
+struct SimtPlan {
+    int mode;
+    int split;  // S (1: no split)
+};
+
+SimtPlan plan_simt(int64_t tiles, int64_t kt_count, int64_t W, const SimtOccupancy &occ)
+{
+    if (W > 0 && tiles < W && kt_count < (int64_t(1) << 28)) {
+        for (int S : kSplitChoices)
+            if (tiles * S <= W && kt_count >= 2 * S && tiles <= occ.clusters[S]) return SimtPlan{kSplit, S};
+    }
+    return SimtPlan{kPlain, 1};
+}
+
+template <bool kVec, int kMode>
+bool launch_clusters(int S, int64_t grid, int64_t tile0, int64_t M, int64_t N, int64_t K, float alpha,
+                     const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                     int64_t ldc, bool vec_c, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sgemm_simt_kernel<kVec, kMode>, M, N, K, alpha, A, lda, B, ldb, beta,
+                              C, ldc, tile0, vec_c) == cudaSuccess;
+}
+
+template <bool kVec>
+bool launch_kernel(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                   const float *B, int64_t ldb, float beta, float *C, int64_t ldc, bool vec_c,
+                   cudaStream_t stream, const DeviceInfo &dev, SimtPlan &pl)
+{
+    int device = 0;
+    cudaGetDevice(&device);
+    const SimtOccupancy &occ = occupancy<kVec>(device);
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    pl = plan_simt(tiles, (K + BK - 1) / BK, static_cast<int64_t>(occ.blocks_per_sm) * dev.sm_count, occ);
+    if (pl.mode == kSplit)
+        return launch_clusters<kVec, kSplit>(pl.split, tiles * pl.split, 0, M, N, K, alpha, A, lda, B, ldb,
+                                             beta, C, ldc, vec_c, stream);
+    sgemm_simt_kernel<kVec, kPlain><<<static_cast<unsigned>(tiles), THREADS, SMEM_BYTES, stream>>>(
+        M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 0, vec_c);
+    return true;
+}
+
+// Variant name of the launch a plan makes.
+const char *simt_name(bool vec, const SimtPlan &pl)
+{
+    static const char *const kPlainName[2] = {"sgemm_simt_128x128x16_ffma2_cpasync4",
+                                              "sgemm_simt_128x128x16_ffma2_cpasync16"};
+    static const char *const kSplitName[2][9] = {
+        {nullptr, nullptr, "sgemm_simt_splitk2_128x128x16_ffma2_cpasync4",
+         "sgemm_simt_splitk3_128x128x16_ffma2_cpasync4", "sgemm_simt_splitk4_128x128x16_ffma2_cpasync4",
+         "sgemm_simt_splitk5_128x128x16_ffma2_cpasync4", nullptr, nullptr,
+         "sgemm_simt_splitk8_128x128x16_ffma2_cpasync4"},
+        {nullptr, nullptr, "sgemm_simt_splitk2_128x128x16_ffma2_cpasync16",
+         "sgemm_simt_splitk3_128x128x16_ffma2_cpasync16", "sgemm_simt_splitk4_128x128x16_ffma2_cpasync16",
+         "sgemm_simt_splitk5_128x128x16_ffma2_cpasync16", nullptr, nullptr,
+         "sgemm_simt_splitk8_128x128x16_ffma2_cpasync16"}};
+    const int v = vec ? 1 : 0;
+    if (pl.mode == kSplit && pl.split >= 2 && pl.split <= 8 && kSplitName[v][pl.split])
+        return kSplitName[v][pl.split];
+    return kPlainName[v];
 }
 
 }  // namespace
 
 const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                               int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-                              int64_t ldc, cudaStream_t stream)
+                              int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
 {
     // 16-byte copies of B need a 16-byte aligned base and row pitch.
     const bool vec_b = aligned16(B) && (ldb % 4 == 0);
     const bool vec_c = aligned16(C) && (ldc % 4 == 0);
-    if (vec_b) {
-        launch_kernel<true>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, vec_c, stream);
-        return "sgemm_simt_128x128x16_ffma2_cpasync16";
-    }
-    launch_kernel<false>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, vec_c, stream);
-    return "sgemm_simt_128x128x16_ffma2_cpasync4";
+    SimtPlan pl{kPlain, 1};
+    const bool ok =
+        vec_b ? launch_kernel<true>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, vec_c, stream, dev, pl)
+              : launch_kernel<false>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, vec_c, stream, dev, pl);
+    // a refused cluster launch is reported through the runtime's error state,
+    // which the caller reads; the name still says what was attempted
+    (void)ok;
+    return simt_name(vec_b, pl);
 }
 
 }  // namespace dgemm

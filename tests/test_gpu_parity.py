@@ -306,3 +306,57 @@ def test_splitk_is_deterministic():
     outs = [parity.run("f16_tn", A, B, C, 1.0, 0.0)[0] for _ in range(3)]
     assert "_splitk" in dg.last_kernel()
     assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+# FP32 SIMT: a problem with fewer tiles than resident CTAs (2 per SM) runs
+# split-K in clusters, the partials added in distributed shared memory.  The
+# expected split assumes GB300's 152 SMs (304 resident CTAs).
+SIMT_SPLIT_CASES = [
+    ((256, 256, 256), "sgemm_simt_splitk8_"),          # 4 tiles, split 8 ways
+    ((100, 1000, 2048), "sgemm_simt_splitk8_"),        # 8 tiles, M tail
+    ((1000, 1000, 3000), "sgemm_simt_splitk4_"),       # 64 tiles, M/N/K tails
+    ((300, 520, 4100), "sgemm_simt_splitk8_"),         # 15 tiles, K tail in the last range
+    ((127, 12288, 640), "sgemm_simt_splitk3_"),        # 96 tiles, skinny
+    ((1200, 1300, 600), "sgemm_simt_splitk2_"),        # 110 tiles
+    ((2048, 2048, 64), "sgemm_simt_128x128"),          # 256 tiles, K too short to split
+    ((4092, 4092, 512), "sgemm_simt_128x128"),         # more tiles than one wave: no split
+]
+
+
+@pytest.mark.parametrize("shape,name", SIMT_SPLIT_CASES)
+def test_simt_split_tail(shape, name):
+    import dense_gemm_09_gb300 as dg
+    M, N, K = shape
+    A, B, C = parity.host_operands("f32", M, N, K, seed=M + 3 * N + K)
+    got, _, _ = parity.run("f32", A, B, C, 1.5, -0.25)
+    assert name in dg.last_kernel(), dg.last_kernel()
+    assert parity.worst_ratio("f32", got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+@pytest.mark.parametrize("shape", [(120, 600, 2048), (1000, 1000, 3000)])
+def test_simt_split_integers_bit_exact(shape):
+    import dense_gemm_09_gb300 as dg
+    M, N, K = shape
+    A, B, C = parity.host_operands("f32", M, N, K, seed=37, dist="int")
+    got, _, _ = parity.run("f32", A, B, C, 1.0, 2.0)
+    assert "splitk" in dg.last_kernel()
+    ref, _ = parity.reference("f32", A, B, C, 1.0, 2.0)
+    assert np.array_equal(got.double().numpy(), ref)
+
+
+def test_simt_split_is_deterministic():
+    import dense_gemm_09_gb300 as dg
+    A, B, C = parity.host_operands("f32", 1000, 1000, 3000, seed=8)
+    outs = [parity.run("f32", A, B, C, 1.0, 0.0)[0] for _ in range(3)]
+    assert "splitk" in dg.last_kernel()
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+def test_simt_split_unaligned_b():
+    # B's pitch is not a multiple of 4 floats: the 4-byte-copy instantiation
+    import dense_gemm_09_gb300 as dg
+    M, N, K = 300, 257, 3001
+    A, B, C = parity.host_operands("f32", M, N, K, seed=41)
+    got, _, _ = parity.run("f32", A, B, C, 1.5, -0.25, pad=(0, 2, 0))
+    assert dg.last_kernel().startswith("sgemm_simt_splitk") and dg.last_kernel().endswith("cpasync4")
+    assert parity.worst_ratio("f32", got, A, B, C, 1.5, -0.25) <= 1.0
