@@ -70,6 +70,8 @@ def lib():
         L.dgemm_test_inject_stall.restype = ci
         L.dgemm_last_kernel.argtypes = []
         L.dgemm_last_kernel.restype = ctypes.c_char_p
+        L.dgemm_tune_next.argtypes = [ci, ci, ci]
+        L.dgemm_tune_next.restype = ci
         _lib = L
         return L
 
@@ -87,6 +89,19 @@ def test_inject_stall(wait_limit_ns: int) -> None:
     """Test hook: the next tensor-core launch on this thread stalls on purpose
     and its bounded waits (limit wait_limit_ns) run out; see include/dgemm.h."""
     lib().dgemm_test_inject_stall(int(wait_limit_ns))
+
+
+# Tile configurations for tune_next (see dgemm_tune_next in include/dgemm.h)
+TUNE_AUTO, TUNE_PAIR, TUNE_SINGLE, TUNE_SPLIT = 0, 1, 2, 3
+
+
+def tune_next(variant: int, bn: int = 256, split: int = 1) -> None:
+    """Tuning hook: fix the tile configuration of the next tensor-core call
+    on this thread (variant TUNE_PAIR / TUNE_SINGLE / TUNE_SPLIT, tile width
+    bn, split-K factor split)."""
+    st = lib().dgemm_tune_next(int(variant), int(bn), int(split))
+    if st != OK:
+        raise DgemmError(st, "dgemm_tune_next")
 
 
 def last_kernel() -> str:

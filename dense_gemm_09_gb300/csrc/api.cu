@@ -171,6 +171,11 @@ extern "C" int dgemm_device_status(int clear)
     return umma_read_status(clear);
 }
 
+extern "C" int dgemm_tune_next(int variant, int bn, int split)
+{
+    return umma_tune_next(variant, bn, split);
+}
+
 extern "C" int dgemm_test_inject_stall(uint64_t wait_limit_ns)
 {
     umma_inject_stall(wait_limit_ns);

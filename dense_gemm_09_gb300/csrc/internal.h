@@ -52,4 +52,7 @@ int umma_read_status(int clear);
 // Test hook behind dgemm_test_inject_stall.
 void umma_inject_stall(uint64_t wait_limit_ns);
 
+// Tuning hook behind dgemm_tune_next.
+int umma_tune_next(int variant, int bn, int split);
+
 }  // namespace dgemm

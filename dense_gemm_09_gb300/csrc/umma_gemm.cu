@@ -39,6 +39,7 @@
 // runs out records DGEMM_ERR_TIMEOUT in the device status word, raises an
 // abort flag that the other roles also poll, waits (again bounded) for its
 // own copies and MMAs in flight, and the CTA releases its TMEM and exits.
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 #include <string>
@@ -190,7 +191,17 @@ struct Params {
     // epilogue stores C through shared-memory boxes and TMA (else direct
     // 16-byte / scalar stores)
     int tma_store;
+    // output tile width of the single-CTA TMA kernel: a multiple of 32 (of 64
+    // for 16-bit N-major B) from 32 to 256; the CTA-pair and register-path
+    // kernels use 256.  The MMA is 128 x bn x UMMA_K.
+    int bn;
 };
+
+// The instruction descriptor with its N field (bits 17-22, N >> 3) set to n.
+__device__ __forceinline__ uint32_t idesc_with_n(uint32_t idesc, int n)
+{
+    return (idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(n >> 3) << 17);
+}
 
 __device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t &m0, int64_t &n0,
                                             int64_t bm = BM)
@@ -202,7 +213,7 @@ __device__ __forceinline__ void tile_coords(int64_t t, const Params &p, int64_t 
     const int64_t g = t / per_group, r = t % per_group;
     const int64_t left = p.tiles_n - g * kGroupN;
     const int64_t gn = left < kGroupN ? left : kGroupN;
-    n0 = (g * kGroupN + r % gn) * BN;
+    n0 = (g * kGroupN + r % gn) * p.bn;
     m0 = (r / gn) * bm;
 }
 
@@ -308,7 +319,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
                 break;
             }
             const uint32_t full = ptx::smem_addr(&ctrl->full[stage]);
-            ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+            ptx::mbar_arrive_expect_tx(full, A_TILE_BYTES + p.bn * ROW_BYTES);
             const uint32_t sa = smem_base + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_TILE_BYTES;
             const int32_t kc = static_cast<int32_t>(kb * T::BK);
@@ -318,8 +329,8 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
             } else {
                 // B is N-major: boxes of 128 bytes of columns x BK rows, one
                 // swizzle column each (see Traits)
-#pragma unroll
-                for (int c = 0; c < BN / T::kNBox; ++c)
+#pragma unroll 1
+                for (int c = 0; c < p.bn / T::kNBox; ++c)
                     ptx::tma_load_2d(sb + c * T::kNBoxBytes, tmap_b, full,
                                      static_cast<int32_t>(n0 + c * T::kNBox), kc);
             }
@@ -526,6 +537,7 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const Sched sc = schedule(p);
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    const uint32_t idesc = kTma ? idesc_with_n(T::kIdesc, p.bn) : T::kIdescKMajorB;
     // test hook: wait on a barrier nothing arrives at, so the wait runs out
     bool ok = !p.inject_stall || wait_bounded(ptx::smem_addr(&ctrl->never), 0, wc);
     for (int64_t t = sc.t0; ok && t < num_tiles; t += sc.dt) {
@@ -557,7 +569,7 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
                     // bytes of columns are kNBoxBytes apart
                     db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
                 }
-                ptx::umma<kKind>(d_tmem, da, db, kTma ? T::kIdesc : T::kIdescKMajorB,
+                ptx::umma<kKind>(d_tmem, da, db, idesc,
                                  (kb != sc.kb0 || k != 0) ? 1u : 0u);
             }
             ptx::umma_commit(ptx::smem_addr(&ctrl->empty[stage]));
@@ -729,7 +741,7 @@ __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *t
     const int64_t row = row0 + lane;
     if (!p.tma_store) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < p.bn / 32; ++c) {
             uint32_t r[32];
             __syncwarp();  // tcgen05.ld is warp-collective (.sync.aligned)
             ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
@@ -740,7 +752,7 @@ __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *t
     }
     constexpr int COLS = box_cols<kKind>();
 #pragma unroll 1
-    for (int b = 0; b < BN / COLS; ++b) {
+    for (int b = 0; b < p.bn / COLS; ++b) {
         const int64_t col0 = n0 + b * COLS;
         uint32_t r[COLS];
         __syncwarp();
@@ -816,38 +828,60 @@ __device__ __forceinline__ void run_epilogue(const Params &p, const CUtensorMap 
 //
 // Each of the S CTAs of a cluster has summed its K range of the same tile in
 // TMEM.  The tile's eight 32-column chunks are owned round-robin: chunk c by
-// rank c mod S.  "push": every CTA copies the chunks it does not own from
-// TMEM straight into the owner's (now idle) stage buffers -- remote stores,
-// which the thread does not wait for.  After a cluster barrier, "reduce":
-// the owner adds, for each row and column, the S partials in rank order
-// 0..S-1 (its own taken from TMEM, the others from its shared memory), so the
-// sum does not depend on timing, and stores alpha * sum + beta * C_old.
-// Layout of the receive buffers: [slot = sender among the other S-1
-// ranks][owned chunk][column j][row], 4-byte words; consecutive threads
-// (rows) touch consecutive words.
+// rank c mod S.  A first cluster barrier, reached by each CTA's epilogue
+// warps only after its accumulator is complete, guarantees that no CTA still
+// reads or fills its stage ring.  "push": every CTA then copies the chunks it
+// does not own from TMEM straight into the owner's idle stage buffers --
+// remote 16-byte stores, which the thread does not wait for.  After a second
+// cluster barrier,
+// "reduce": the owner adds, for each row and column, the S partials in rank
+// order 0..S-1 (its own taken from TMEM, the others from its shared memory),
+// so the sum does not depend on timing, and stores alpha * sum + beta * C_old.
+// Nothing crosses CTAs after that barrier, so each CTA leaves when its own
+// reduction is done.
+// Layout of the receive buffers, in 16-byte units: [slot = sender among the
+// other S-1 ranks][owned chunk][column quad q][row]; consecutive threads
+// (rows) touch consecutive 16-byte words, so a warp moves 512 contiguous
+// bytes per access.
+
+constexpr uint32_t splitk_recv_bytes(uint32_t S)
+{
+    return (S - 1) * ((BN / 32 + S - 1) / S) * 8u * BM * 16u;
+}
+static_assert(splitk_recv_bytes(2) <= STAGES * STAGE_BYTES && splitk_recv_bytes(3) <= STAGES * STAGE_BYTES &&
+                  splitk_recv_bytes(4) <= STAGES * STAGE_BYTES && splitk_recv_bytes(5) <= STAGES * STAGE_BYTES &&
+                  splitk_recv_bytes(6) <= STAGES * STAGE_BYTES && splitk_recv_bytes(7) <= STAGES * STAGE_BYTES &&
+                  splitk_recv_bytes(8) <= STAGES * STAGE_BYTES,
+              "split-K partials must fit in the stage ring");
 
 __device__ __forceinline__ uint32_t recv_offset(uint32_t slot, uint32_t chunk_idx, uint32_t S,
-                                                int j, int row)
+                                                int q, int row)
 {
     const uint32_t owned_max = (BN / 32 + S - 1) / S;
-    return (((slot * owned_max + chunk_idx) * 32u + static_cast<uint32_t>(j)) * BM +
-            static_cast<uint32_t>(row)) * 4u;
+    return (((slot * owned_max + chunk_idx) * 8u + static_cast<uint32_t>(q)) * BM +
+            static_cast<uint32_t>(row)) * 16u;
 }
 
-__device__ __forceinline__ void splitk_push(const Params &p, Ctrl *ctrl, uint32_t tmem_base,
-                                            uint32_t smem_base, int warp, int lane, WaitCtl *wc)
+// The accumulator of this CTA's K range is complete (its MMAs, and with them
+// every read of its stage ring, are done).  Bounded; a time-out raises the
+// CTA's abort flag, which push and reduce check.
+__device__ __forceinline__ void splitk_wait_acc(Ctrl *ctrl, WaitCtl *wc)
+{
+    wait_bounded(ptx::smem_addr(&ctrl->tmem_full[0]), 0, wc);
+}
+
+__device__ __forceinline__ void splitk_push(const Params &p, uint32_t tmem_base, uint32_t smem_base,
+                                            int warp, int lane, WaitCtl *wc)
 {
     const uint32_t quarter = static_cast<uint32_t>(warp & 3);
-    bool ok = wait_bounded(ptx::smem_addr(&ctrl->tmem_full[0]), 0, wc);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) return;
+    if (__any_sync(0xffffffffu, aborted(wc))) return;
     ptx::tc_fence_after();
     const uint32_t S = static_cast<uint32_t>(p.splitk);
     const uint32_t rank = ptx::cluster_ctarank();
     const int row = static_cast<int>(quarter * 32 + lane);
     const uint32_t taddr = tmem_base + ((quarter * 32u) << 16);
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 0; c < p.bn / 32; ++c) {
         const uint32_t owner = static_cast<uint32_t>(c) % S;
         if (owner == rank) continue;
         uint32_t r[32];
@@ -858,8 +892,10 @@ __device__ __forceinline__ void splitk_push(const Params &p, Ctrl *ctrl, uint32_
         const uint32_t base = ptx::mapa(smem_base + recv_offset(slot, static_cast<uint32_t>(c) / S, S, 0, row),
                                         owner);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            ptx::st_shared_cluster_f32(base + static_cast<uint32_t>(j) * BM * 4u, __uint_as_float(r[j]));
+        for (int q = 0; q < 8; ++q)
+            ptx::st_shared_cluster_v4(base + static_cast<uint32_t>(q) * BM * 16u,
+                                      make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                  __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
     }
 }
 
@@ -877,7 +913,7 @@ __device__ __forceinline__ void splitk_reduce(const Params &p, uint32_t tmem_bas
     const uint32_t taddr = tmem_base + ((quarter * 32u) << 16);
     ptx::tc_fence_after();
 #pragma unroll 1
-    for (uint32_t c = rank; c < BN / 32; c += S) {
+    for (uint32_t c = rank; c < static_cast<uint32_t>(p.bn) / 32; c += S) {
         uint32_t own[32];
         __syncwarp();
         ptx::tmem_ld_32x32b_x32(taddr + c * 32, own);
@@ -893,8 +929,13 @@ __device__ __forceinline__ void splitk_reduce(const Params &p, uint32_t tmem_bas
                 const uint32_t slot = q < rank ? q : q - 1;
                 const uint32_t base = smem_base + recv_offset(slot, c / S, S, 0, row);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    acc[j] += ptx::ld_shared_f32(base + static_cast<uint32_t>(j) * BM * 4u);
+                for (int v = 0; v < 8; ++v) {
+                    const float4 f = ptx::ld_shared_v4f(base + static_cast<uint32_t>(v) * BM * 16u);
+                    acc[4 * v] += f.x;
+                    acc[4 * v + 1] += f.y;
+                    acc[4 * v + 2] += f.z;
+                    acc[4 * v + 3] += f.w;
+                }
             }
         }
         uint32_t r[32];
@@ -972,7 +1013,7 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
         if (lane == 0) run_mma<kKind, kTma>(p, smem_base, ctrl, tmem_base, wc);
     } else {
         if (p.splitk > 1)
-            splitk_push(p, ctrl, tmem_base, smem_base, warp, lane, wc);
+            splitk_wait_acc(ctrl, wc);
         else
             run_epilogue<kKind>(p, &tmap_c, ctrl, tmem_base, smem_base + STAGES * STAGE_BYTES, warp,
                                 lane, wc);
@@ -981,10 +1022,12 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
     if (p.splitk > 1) {  // uniform over the cluster
         __syncwarp();
         ptx::tc_fence_before();
+        ptx::cluster_sync();  // every CTA's accumulator is complete: all stage rings are idle
+        if (warp > kMmaWarp) splitk_push(p, tmem_base, smem_base, warp, lane, wc);
+        __syncwarp();
+        ptx::tc_fence_before();
         ptx::cluster_sync();  // every pushed partial has landed in its owner
         if (warp > kMmaWarp) splitk_reduce<kKind>(p, tmem_base, smem_base, warp, lane, wc);
-        __syncwarp();
-        ptx::cluster_sync();  // keep the cluster together until every owner is done
     }
 
     __syncwarp();
@@ -1353,6 +1396,8 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, 
                    const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int bk, bool vec_c)
 {
     Params p;
+    p.bn = BN;
+    p.tma_store = 0;
     p.inject_stall = t_inject_limit_ns ? 1 : 0;
     p.splitk = 1;
     p.wait_limit_ns = t_inject_limit_ns ? t_inject_limit_ns : kWaitLimitNs;
@@ -1420,17 +1465,76 @@ int cluster_capacity(int size)
 // Split factor for problems with few output tiles: the largest S <= 8 (the
 // portable cluster size) such that every range has at least 8 K blocks and
 // all tiles x S CTAs are resident in one wave of clusters.  1 = no split.
+// Tile configuration of one call: the CTA-pair kernel (256 x 256 tiles), the
+// persistent single-CTA kernel (128 x bn tiles) or split-K over S CTAs of a
+// cluster (128 x bn tiles).
+enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3 };
+struct UmmaConfig {
+    int variant;
+    int bn;
+    int split;
+};
+
+// One-shot override of the next call on this host thread (dgemm_tune_next).
+thread_local UmmaConfig t_tune = {kVariantAuto, BN, 1};
+
+// Narrowest tile width step of a kind: the N-major 16-bit kinds load B in
+// 64-column boxes; the others take any multiple of 32.
 template <int kKind>
-int choose_splitk(const Params &p, int sm_count)
+constexpr int bn_step()
 {
-    const int64_t tiles = p.tiles_m * p.tiles_n;  // single-CTA 128 x 256 tiles
-    if (tiles * 2 > sm_count) return 1;
-    int64_t s = sm_count / tiles;
-    if (s > p.num_kb / 8) s = p.num_kb / 8;
-    if (s > 8) s = 8;
-    for (; s >= 2; --s)
-        if (tiles <= cluster_capacity<kKind>(static_cast<int>(s))) return static_cast<int>(s);
-    return 1;
+    return Traits<kKind>::kBNMajor ? Traits<kKind>::kNBox : 32;
+}
+
+// Automatic choice.  Problems with more than one wave of 128 x 256 tiles
+// take the pair kernel (M > 128); between half a wave and one wave, the
+// single-CTA kernel with 256-wide tiles.  Smaller ones -- skinny M, or few
+// tiles and a long K -- choose the
+// tile width bn and the split S that keep the most SMs streaming:
+//   * candidates: bn from 256 down in the kind's step (32, or 64 for the
+//     16-bit NN kinds); S from 1 to 8 with at least 8 K blocks per rank,
+//     tiles * S <= SMs, and all clusters resident at once;
+//   * estimated time per CTA = its K blocks x max(MMA time, load time) +
+//     the cost of adding S partials, with the load time of a K block
+//     (128 + bn rows of 128 bytes) at a per-SM stream rate and the whole
+//     launch no faster than the operands at the HBM rate;
+//   * the smallest estimate wins (ties: the wider tile, the smaller S).
+// The constants are fitted to GB300 sweeps of the tuning tool
+// (dense_gemm_09_gb300/tune.py): an MMA K block of 128 x 256 x 128 bytes in
+// ~0.33 us, a CTA streams ~75 GB/s, HBM ~6 TB/s; a split costs ~1 us plus
+// ~0.5 us per extra rank plus ~0.9 us per 64 KB of partials moved.
+template <int kKind>
+UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok)
+{
+    using T = Traits<kKind>;
+    const int64_t tiles256 = p.tiles_m * ((p.N + BN - 1) / BN);
+    // more than one wave of 128 x 256 tiles: the pair halves each CTA's
+    // operand traffic; within one wave the single-CTA kernel is as fast and
+    // has less to synchronise (2048^3 FP16: 21.2 us single, 22.9 us pair)
+    if (tiles256 > sm_count) return {pair_ok && p.M > BM ? kVariantPair : kVariantSingle, BN, 1};
+    if (tiles256 * 2 > sm_count) return {kVariantSingle, BN, 1};
+    const double kb_mma_us = 0.33 / 256.0;          // per column of bn, one K block
+    const double sm_bytes_per_us = 75e3;            // 75 GB/s
+    const double hbm_bytes_per_us = 6.0e6;          // 6 TB/s
+    const double operand_bytes = static_cast<double>(p.M * p.K + p.N * p.K) * T::kElem;
+    UmmaConfig best{kVariantSingle, BN, 1};
+    double best_t = 1e30;
+    for (int bn = BN; bn >= bn_step<kKind>(); bn -= bn_step<kKind>()) {
+        const int64_t tiles = p.tiles_m * ((p.N + bn - 1) / bn);
+        for (int S = 1; S <= 8; ++S) {
+            if (tiles * S > sm_count) break;
+            if (S > 1 && (p.num_kb < 8 * S || tiles > cluster_capacity<kKind>(S))) continue;
+            const int64_t kb = (p.num_kb + S - 1) / S;
+            const double t_kb = std::max(kb_mma_us * bn, (BM + bn) * 128.0 / sm_bytes_per_us);
+            double t = std::max(kb * t_kb, operand_bytes / hbm_bytes_per_us);
+            if (S > 1) t += 1.0 + 0.5 * (S - 1) + 0.9 * (BM * bn * 4.0 / 65536.0) * (S - 1) / S;
+            if (t < best_t * 0.98) {
+                best_t = t;
+                best = {S > 1 ? kVariantSplit : kVariantSingle, bn, S};
+            }
+        }
+    }
+    return best;
 }
 
 template <int kKind>
@@ -1461,11 +1565,13 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorM
     return true;
 }
 
-// Variant names ("umma_<kind>_<variant>"), built once per kind.
+// Variant names ("umma_<kind>_<variant>"), built once per kind:
+// [0] pair, [1] register / cp.async producer, then per tile width bn
+// (32..256) the single-CTA TMA kernel and split-K S = 2..8.
 template <int kKind>
-const char *variant_name(int variant, int split)
+const char *variant_name(int variant, int bn = BN, int split = 1)
 {
-    static std::string names[12];  // 0 pair, 1 single TMA, 2 register / cp.async, 3+S split-K
+    static std::string names[2 + 9 * 9];
     static std::once_flag once;
     std::call_once(once, [] {
         using T = Traits<kKind>;
@@ -1474,36 +1580,56 @@ const char *variant_name(int variant, int split)
         const std::string bk = std::to_string(T::BK);
         const std::string base = std::string("umma_") + kind;
         names[0] = base + "_pair_256x256x" + bk + "_tma";
-        names[1] = base + "_128x256x" + bk + "_tma";
-        names[2] = base + "_128x256x" + bk + (kKind == kTF32 ? "_cpasync" : "_ldst");
-        for (int S = 2; S <= 8; ++S)
-            names[3 + S] = base + "_splitk" + std::to_string(S) + "_128x256x" + bk + "_tma";
+        names[1] = base + "_128x256x" + bk + (kKind == kTF32 ? "_cpasync" : "_ldst");
+        for (int w = 1; w <= 8; ++w) {
+            const std::string tile = "128x" + std::to_string(32 * w) + "x" + bk;
+            names[2 + w * 9 + 1] = base + "_" + tile + "_tma";
+            for (int S = 2; S <= 8; ++S)
+                names[2 + w * 9 + S] = base + "_splitk" + std::to_string(S) + "_" + tile + "_tma";
+        }
     });
-    return names[variant == 3 ? 3 + split : variant].c_str();
+    if (variant == kVariantPair) return names[0].c_str();
+    if (variant == kVariantAuto) return names[1].c_str();  // the non-TMA kernel
+    const int w = bn / 32, S = variant == kVariantSplit ? split : 1;
+    return names[2 + w * 9 + S].c_str();
 }
 
-// TMA-capable operands: split-K for few tiles, CTA pairs for M > 128, else
-// the persistent single-CTA kernel.  ma / mb: maps with the single-CTA boxes;
-// mb_pair: B with 128-row boxes.
-template <int kKind>
-const char *dispatch_tma(const Params &p, const CUtensorMap &ma, const CUtensorMap &mb,
-                         const CUtensorMap *mb_pair, const CUtensorMap &mc, cudaStream_t stream,
-                         const DeviceInfo &dev)
+// TMA-capable operands.  ma: A with 128-row boxes; mb_pair: B boxes of the
+// pair kernel (null if B cannot be described); make_b(bn, map) builds B's map
+// for 128 x bn tiles.
+template <int kKind, typename MakeB>
+const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *mb_pair,
+                         MakeB make_b, const CUtensorMap &mc, cudaStream_t stream, const DeviceInfo &dev)
 {
-    const char *pair_name = variant_name<kKind>(0, 0);
-    const char *single_name = variant_name<kKind>(1, 0);
-    const int S = choose_splitk<kKind>(p, dev.sm_count);
-    if (S > 1) {
-        Params ps = p;
-        ps.splitk = S;
-        if (launch_splitk<kKind>(ma, mb, mc, ps, stream)) return variant_name<kKind>(3, S);
+    UmmaConfig cfg = t_tune;
+    t_tune = UmmaConfig{kVariantAuto, BN, 1};
+    if ((cfg.variant == kVariantPair && !mb_pair) || cfg.bn % bn_step<kKind>() != 0)
+        cfg.variant = kVariantAuto;
+    // every rank of a split needs at least one K block
+    if (cfg.variant == kVariantSplit && cfg.split > p0.num_kb)
+        cfg = p0.num_kb >= 2 ? UmmaConfig{kVariantSplit, cfg.bn, static_cast<int>(p0.num_kb)}
+                             : UmmaConfig{kVariantSingle, cfg.bn, 1};
+    if (cfg.variant == kVariantAuto) cfg = choose_config<kKind>(p0, dev.sm_count, mb_pair != nullptr);
+    Params p = p0;
+    if (cfg.variant == kVariantPair) {
+        p.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
+        if (launch_pair<kKind>(ma, *mb_pair, mc, p, stream)) return variant_name<kKind>(kVariantPair);
+        cfg = UmmaConfig{kVariantSingle, BN, 1};
+        p = p0;
     }
-    if (mb_pair && p.M > BM) {
-        Params pp = p;
-        pp.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
-        if (launch_pair<kKind>(ma, *mb_pair, mc, pp, stream)) return pair_name;
+    p.bn = cfg.bn;
+    p.tiles_n = (p.N + cfg.bn - 1) / cfg.bn;
+    if (p.bn % box_cols<kKind>() != 0) p.tma_store = 0;
+    CUtensorMap mb{};
+    if (!make_b(cfg.bn, &mb)) return nullptr;
+    if (cfg.variant == kVariantSplit) {
+        p.splitk = cfg.split;
+        if (launch_splitk<kKind>(ma, mb, mc, p, stream))
+            return variant_name<kKind>(kVariantSplit, cfg.bn, cfg.split);
+        p.splitk = 1;
     }
-    return launch<kKind, true>(ma, mb, mc, p, stream, dev) ? single_name : nullptr;
+    return launch<kKind, true>(ma, mb, mc, p, stream, dev) ? variant_name<kKind>(kVariantSingle, cfg.bn)
+                                                           : nullptr;
 }
 
 template <int kKind>
@@ -1524,24 +1650,27 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
                       ? 1 : 0;
     // TMA needs 16-byte aligned bases and row pitches.
     const bool tma = aligned16(A) && aligned16(B) && (lda * es) % 16 == 0 && (ldb * es) % 16 == 0;
-    CUtensorMap ma{}, mb{}, mbp{};
+    CUtensorMap ma{}, mbp{};
     if (tma && make_map(&ma, dt, A, K, M, lda * es, T::BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) {
-        bool ok_b, ok_pair;
-        if constexpr (T::kBNMajor) {
-            // B stored K x N: boxes of 128 bytes of columns x BK rows, shared
-            // by the single-CTA and pair kernels
-            ok_b = make_map(&mb, dt, B, N, K, ldb * es, T::kNBox, T::BK,
-                            T::kTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
-            mbp = mb;
-            ok_pair = ok_b;
-        } else {
-            // B stored N x K: BN-row boxes (single CTA), 128-row boxes (pair)
-            ok_b = make_map(&mb, dt, B, K, N, ldb * es, T::BK, BN, CU_TENSOR_MAP_SWIZZLE_128B);
-            ok_pair = make_map(&mbp, dt, B, K, N, ldb * es, T::BK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        // B stored K x N: boxes of 128 bytes of columns x BK rows, whatever the
+        // tile width; B stored N x K: bn-row boxes (single CTA), 128-row boxes
+        // (pair)
+        auto make_b = [&](int bn, CUtensorMap *m) {
+            if constexpr (T::kBNMajor)
+                return make_map(m, dt, B, N, K, ldb * es, T::kNBox, T::BK,
+                                T::kTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
+            else
+                return make_map(m, dt, B, K, N, ldb * es, T::BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+        };
+        CUtensorMap probe{};
+        if (make_b(BN, &probe)) {
+            const bool ok_pair = make_b(128, &mbp);
+            return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, make_b, mc, stream, dev);
         }
-        if (ok_b) return dispatch_tma<kKind>(p, ma, mb, ok_pair ? &mbp : nullptr, mc, stream, dev);
     }
-    return launch<kKind, false>(ma, mb, mc, p, stream, dev) ? variant_name<kKind>(2, 0) : nullptr;
+    t_tune = UmmaConfig{kVariantAuto, BN, 1};
+    CUtensorMap mb{};
+    return launch<kKind, false>(ma, mb, mc, p, stream, dev) ? variant_name<kKind>(kVariantAuto) : nullptr;
 }
 
 }  // namespace
@@ -1564,6 +1693,15 @@ const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, 
     default:
         return nullptr;
     }
+}
+
+int umma_tune_next(int variant, int bn, int split)
+{
+    if (variant < kVariantAuto || variant > kVariantSplit) return DGEMM_ERR_INVALID_ARG;
+    if (variant >= kVariantSingle && (bn < 32 || bn > BN || bn % 32 != 0)) return DGEMM_ERR_INVALID_ARG;
+    if (variant == kVariantSplit && (split < 2 || split > 8)) return DGEMM_ERR_INVALID_ARG;
+    t_tune = UmmaConfig{variant, variant >= kVariantSingle ? bn : BN, variant == kVariantSplit ? split : 1};
+    return DGEMM_OK;
 }
 
 void umma_inject_stall(uint64_t wait_limit_ns)

@@ -1,0 +1,113 @@
+"""Tile-configuration sweep for the tensor-core calls.
+
+For one problem shape and kind, times the automatic choice and every tile
+configuration the library can run -- the CTA-pair kernel, the single-CTA
+kernel at each tile width bn, and split-K at each (bn, S) -- and prints them
+fastest first, with each result's largest difference from the automatic
+choice (relative to max |C|).  This is the search over tile parameters per
+problem that "如何优化一个 CUDA Matmul Kernel ... Worklog" runs in "Kernel 9:
+Autotuning"; the library's automatic choice is a cost model fitted to such
+sweeps.
+
+    python -m dense_gemm_09_gb300.tune --kind f16_tn --shape 127x12288x4096
+
+Operands are seeded uniform[-1, 1) values on the current GPU; the L2 cache
+is flushed before every timed call, and times are means of CUDA-event
+intervals (the event clock ticks in steps of about 2 us, so means resolve
+finer differences than medians).
+"""
+from __future__ import annotations
+
+import argparse
+import statistics
+
+import torch
+
+import dense_gemm_09_gb300 as dg
+
+KINDS = {
+    "tf32": (torch.float32, False, dg.gemm_tf32, 32),
+    "f16_tn": (torch.float16, True, dg.gemm_f16_tn, 32),
+    "f16_nn": (torch.float16, False, dg.gemm_f16_nn, 64),
+    "bf16_tn": (torch.bfloat16, True, dg.gemm_bf16_tn, 32),
+    "bf16_nn": (torch.bfloat16, False, dg.gemm_bf16_nn, 64),
+}
+
+
+def configs(step: int, sms: int, M: int, N: int):
+    """Every (variant, bn, split) worth timing: the pair kernel, and for each
+    tile width bn the single-CTA kernel and the splits that fit one wave."""
+    out = [(dg.TUNE_AUTO, 256, 1), (dg.TUNE_PAIR, 256, 1)]
+    tiles_m = (M + 127) // 128
+    for bn in range(256, 31, -step):
+        out.append((dg.TUNE_SINGLE, bn, 1))
+        tiles = tiles_m * ((N + bn - 1) // bn)
+        for S in range(2, 9):
+            if tiles * S <= sms:
+                out.append((dg.TUNE_SPLIT, bn, S))
+    return out
+
+
+def sweep(kind: str, M: int, N: int, K: int, reps: int = 30, warmup: int = 3, seed: int = 0):
+    dtype, tn, fn, step = KINDS[kind]
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(seed)
+    A = (torch.rand((M, K), generator=g) * 2 - 1).to(dtype).to(dev)
+    Bshape = (N, K) if tn else (K, N)
+    B = (torch.rand(Bshape, generator=g) * 2 - 1).to(dtype).to(dev)
+    C = torch.empty((M, N), dtype=dtype, device=dev)
+    flush = torch.empty(512 * 2**20 // 4, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ref = None
+    rows = []
+    for variant, bn, split in configs(step, sms, M, N):
+        def call():
+            if variant != dg.TUNE_AUTO:
+                dg.tune_next(variant, bn, split)
+            fn(A, B, C, 1.0, 0.0)
+        for _ in range(warmup):
+            call()
+        times = []
+        for _ in range(reps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        name = dg.last_kernel()
+        out = C.float()
+        if ref is None:
+            ref = out.clone()
+            scale = max(ref.abs().max().item(), 1e-30)
+        diff = (out - ref).abs().max().item() / scale
+        ms = statistics.mean(times)
+        rows.append((ms, name, variant == dg.TUNE_AUTO, diff))
+    assert dg.device_status() == dg.OK
+    auto_name = rows[0][1]
+    best = {}  # one line per kernel actually run (a request the call cannot take runs the automatic one)
+    for ms, name, _, diff in rows:
+        if name not in best or ms < best[name][0]:
+            best[name] = (ms, diff)
+    return sorted((ms, name, name == auto_name, diff) for name, (ms, diff) in best.items())
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--kind", choices=sorted(KINDS), default="f16_tn")
+    ap.add_argument("--shape", required=True, help="MxNxK")
+    ap.add_argument("--reps", type=int, default=30)
+    a = ap.parse_args()
+    M, N, K = (int(v) for v in a.shape.lower().split("x"))
+    table = sweep(a.kind, M, N, K, reps=a.reps)
+    flops = 2.0 * M * N * K
+    print("%s %dx%dx%d" % (a.kind, M, N, K))
+    for ms, name, auto, diff in table:
+        print("  %-44s %9.4f ms %9.2f TFLOP/s  max rel diff %.1e%s"
+              % (name, ms, flops / ms / 1e9, diff, "   <- automatic" if auto else ""))
+
+
+if __name__ == "__main__":
+    main()

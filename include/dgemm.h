@@ -173,6 +173,29 @@ int dgemm_device_status(int clear);
 int dgemm_test_inject_stall(uint64_t wait_limit_ns);
 
 /*
+ * dgemm_tune_next -- TUNING HOOK.  Fixes the tile configuration of the next
+ * tensor-core call (gemm_tf32, gemm_f16_*, gemm_bf16_*) made by the calling
+ * host thread; one call only, after which the automatic choice resumes.
+ *   variant 0: automatic (the default);
+ *           1: CTA pair, 256 x 256 output tiles;
+ *           2: one CTA per 128 x bn tile, persistent grid;
+ *           3: split-K, `split` CTAs of a cluster per 128 x bn tile.
+ *   bn:    tile width for variants 2 and 3: 32..256 in steps of 32; the
+ *          NN 16-bit calls need a multiple of 64.  Ignored otherwise.
+ *   split: 2..8 for variant 3 (lowered to the number of K blocks when K is
+ *          shorter, so that every CTA has work); ignored otherwise.
+ * Returns DGEMM_ERR_INVALID_ARG (and records nothing) for values outside
+ * these ranges, else DGEMM_OK.  A configuration the next call cannot take
+ * (operands that only the register-path kernel can load, or a bn that is not
+ * a multiple of the call's step) is ignored, and the call chooses as usual;
+ * dgemm_last_kernel() names what ran.  Results agree with the automatic
+ * choice up to the order of the FP32 additions of split partials.  Source:
+ * "如何优化一个 CUDA Matmul Kernel ... Worklog", section "Kernel 9:
+ * Autotuning" (searching tile parameters per problem instead of fixing one).
+ */
+int dgemm_tune_next(int variant, int bn, int split);
+
+/*
  * dgemm_last_kernel -- name of the kernel variant the last successful call
  * on this host thread launched ("" if none): for tests and the benchmark.
  */

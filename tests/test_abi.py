@@ -109,3 +109,15 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 def test_last_kernel_empty_before_any_launch(L):
     assert L.dgemm_last_kernel() == b""
+
+
+def test_tune_next_validates_on_host(L):
+    # out-of-range requests are refused and record nothing (no device needed)
+    assert L.dgemm_tune_next(-1, 256, 1) == 1
+    assert L.dgemm_tune_next(4, 256, 1) == 1
+    assert L.dgemm_tune_next(2, 48, 1) == 1      # bn not a multiple of 32
+    assert L.dgemm_tune_next(2, 288, 1) == 1     # bn above 256
+    assert L.dgemm_tune_next(3, 128, 1) == 1     # split below 2
+    assert L.dgemm_tune_next(3, 128, 9) == 1     # split above 8
+    assert L.dgemm_tune_next(3, 128, 4) == 0
+    assert L.dgemm_tune_next(0, 0, 0) == 0       # back to automatic

@@ -245,21 +245,28 @@ def test_kernel_variant_names(path):
     want = "sgemm_simt" if path == "f32" else "umma_" + path
     assert dg.last_kernel().startswith(want)
     if path != "f32":
-        # M > 128 and 16-byte pitches: the CTA-pair kernel
-        assert dg.last_kernel().endswith("_tma") and "_pair_" in dg.last_kernel()
-        A, B, C = parity.host_operands(path, 128, 256, 256, seed=1)
+        # more than one wave of 128 x 256 tiles with M > 128: the CTA pair
+        A, B, C = parity.host_operands(path, 2560, 2048, 64, seed=1)
         got, _, _ = parity.run(path, A, B, C, 1.0, 0.0)
-        assert dg.last_kernel().endswith("_tma") and "_pair_" not in dg.last_kernel()
+        assert dg.last_kernel().endswith("_tma") and "_pair_" in dg.last_kernel()
+        assert parity.worst_ratio(path, got, A, B, C, 1.0, 0.0) <= 1.0
+        # half a wave to one wave of tiles: the single-CTA kernel, 256 wide
+        A, B, C = parity.host_operands(path, 128, 20480, 64, seed=1)
+        got, _, _ = parity.run(path, A, B, C, 1.0, 0.0)
+        assert "_128x256x" in dg.last_kernel() and dg.last_kernel().endswith("_tma")
         assert parity.worst_ratio(path, got, A, B, C, 1.0, 0.0) <= 1.0
 
 
 @pytest.mark.parametrize("path", parity.TC_PATHS)
 @pytest.mark.parametrize("M", [129, 200, 255, 256, 257, 383, 511, 640])
 def test_pair_kernel_m_tails(path, M):
+    import dense_gemm_09_gb300 as dg
     # the pair tile is 256 rows: the odd CTA's rows run past M in these cases
     N, K = 520, 264
     A, B, C = parity.host_operands(path, M, N, K, seed=M)
+    dg.tune_next(dg.TUNE_PAIR)  # few tiles: the automatic choice would take the single-CTA kernel
     got, _, _ = parity.run(path, A, B, C, 1.5, -0.25)
+    assert "_pair_" in dg.last_kernel()
     assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
 
 
@@ -360,3 +367,50 @@ def test_simt_split_unaligned_b():
     got, _, _ = parity.run("f32", A, B, C, 1.5, -0.25, pad=(0, 2, 0))
     assert dg.last_kernel().startswith("sgemm_simt_splitk") and dg.last_kernel().endswith("cpasync4")
     assert parity.worst_ratio("f32", got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+# The tuning hook: every tile configuration the sweep tool can request gives
+# a correct result (narrow tiles, tiles whose width is not a multiple of the
+# TMA-store box, every split factor, and splits wider than K allows).
+def _tune_cases():
+    import dense_gemm_09_gb300 as dg
+    cases = []
+    for path in ("f16_tn", "tf32"):
+        cases += [(path, (300, 1000, 1024), dg.TUNE_PAIR, 256, 1)]
+        cases += [(path, (200, 1000, 1024), dg.TUNE_SINGLE, bn, 1) for bn in (32, 96, 160, 224, 256)]
+        cases += [(path, (127, 1000, 2048), dg.TUNE_SPLIT, bn, S) for bn, S in
+                  ((32, 2), (96, 3), (128, 4), (160, 5), (192, 6), (224, 7), (256, 8))]
+        cases += [(path, (100, 300, 200), dg.TUNE_SPLIT, 64, 8)]  # 4 or 7 K blocks: S lowered
+    # N = 520 keeps the NN kinds' B pitch a multiple of 16 bytes (TMA, so the pair can run)
+    cases += [(path, (255, 520, 304), dg.TUNE_PAIR, 256, 1) for path in parity.TC_PATHS]
+    cases += [("f16_nn", (200, 1000, 1024), dg.TUNE_SINGLE, 192, 1),
+              ("f16_nn", (127, 1000, 2048), dg.TUNE_SPLIT, 128, 3),
+              ("bf16_nn", (127, 1000, 2048), dg.TUNE_SPLIT, 64, 2),
+              ("bf16_tn", (200, 1000, 1024), dg.TUNE_SINGLE, 96, 1)]
+    return cases
+
+
+@pytest.mark.parametrize("path,shape,variant,bn,split", _tune_cases())
+def test_tuned_configurations(path, shape, variant, bn, split):
+    import dense_gemm_09_gb300 as dg
+    M, N, K = shape
+    A, B, C = parity.host_operands(path, M, N, K, seed=M + N + bn + split)
+    dg.tune_next(variant, bn, split)
+    got, _, _ = parity.run(path, A, B, C, 1.5, -0.25)
+    name = dg.last_kernel()
+    if variant == dg.TUNE_PAIR:
+        assert "_pair_" in name
+    else:
+        assert ("_128x%dx" % bn) in name, name
+        assert ("_splitk" in name) == (variant == dg.TUNE_SPLIT), name
+    assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+def test_tuning_is_one_shot():
+    import dense_gemm_09_gb300 as dg
+    A, B, C = parity.host_operands("f16_tn", 127, 1000, 2048, seed=6)
+    dg.tune_next(dg.TUNE_PAIR)
+    parity.run("f16_tn", A, B, C, 1.0, 0.0)
+    assert "_pair_" in dg.last_kernel()
+    parity.run("f16_tn", A, B, C, 1.0, 0.0)  # M = 127: the automatic choice is never the pair
+    assert "_pair_" not in dg.last_kernel()

@@ -14,18 +14,21 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
+# (path, shape, pitch padding, tile configuration forced through the tuning
+# hook or None for the automatic choice, expected variant name fragment)
 CASES = [
-    ("f16_tn", (256, 512, 256), (0, 0, 0), "_pair_"),     # CTA-pair kernel
-    ("tf32", (256, 512, 256), (0, 0, 0), "_pair_"),
-    ("f16_tn", (128, 512, 256), (0, 0, 0), "_128x256x64_tma"),   # single-CTA kernel
-    ("tf32", (100, 260, 36), (1, 0, 0), "_cpasync"),      # cp.async producer (unaligned TF32)
-    ("f16_tn", (100, 260, 36), (1, 0, 0), "_ldst"),       # register-path producer (unaligned FP16)
-    ("f16_tn", (100, 1000, 2048), (0, 0, 0), "_splitk"),  # split-K cluster kernel
+    ("f16_tn", (256, 512, 256), (0, 0, 0), "pair", "_pair_"),             # CTA-pair kernel
+    ("tf32", (256, 512, 256), (0, 0, 0), "pair", "_pair_"),
+    ("f16_tn", (128, 512, 256), (0, 0, 0), "single", "_128x256x64_tma"),  # single-CTA kernel
+    ("tf32", (100, 260, 36), (1, 0, 0), None, "_cpasync"),    # cp.async producer (unaligned TF32)
+    ("f16_tn", (100, 260, 36), (1, 0, 0), None, "_ldst"),     # register-path producer (unaligned FP16)
+    ("f16_tn", (100, 1000, 2048), (0, 0, 0), None, "_splitk"),  # split-K cluster kernel
 ]
 
 
-@pytest.mark.parametrize("path,shape,pad,variant", CASES, ids=[c[3].strip("_") + "-" + c[0] for c in CASES])
-def test_stalled_launch_times_out_cleanly(path, shape, pad, variant):
+@pytest.mark.parametrize("path,shape,pad,force,variant", CASES,
+                         ids=[c[4].strip("_") + "-" + c[0] for c in CASES])
+def test_stalled_launch_times_out_cleanly(path, shape, pad, force, variant):
     import dense_gemm_09_gb300 as dg
     M, N, K = shape
     A, B, C = parity.host_operands(path, M, N, K, seed=3)
@@ -36,11 +39,15 @@ def test_stalled_launch_times_out_cleanly(path, shape, pad, variant):
     assert dg.device_status(clear=True) == dg.OK
     fn = {"tf32": dg.gemm_tf32, "f16_tn": dg.gemm_f16_tn}[path]
 
+    if force == "pair":
+        dg.tune_next(dg.TUNE_PAIR)
+    elif force == "single":
+        dg.tune_next(dg.TUNE_SINGLE, 256)
     dg.test_inject_stall(20_000_000)  # 20 ms
     t0 = time.monotonic()
     fn(dA, dB, dC, 1.0, 0.0)
+    st = dg.device_status(clear=True)  # synchronises (and clears before any assert below)
     assert variant in dg.last_kernel()
-    st = dg.device_status(clear=True)  # synchronises
     elapsed = time.monotonic() - t0
     assert st == dg.ERR_TIMEOUT, dg.status_string(st)
     assert elapsed < 10.0
