@@ -105,6 +105,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// 3-D form of tma_load_2d_pair (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap, uint32_t bar_cluster,
+                                                 int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // Tile store shared -> global (bulk-group completion); the box must start on
 // a 16-byte boundary in its innermost coordinate and at non-negative
 // coordinates.  Elements outside the tensor are not written.
@@ -253,6 +264,22 @@ __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
+}
+
+// Named CTA barrier `id` over `count` threads (whole warps) that also ORs a
+// predicate across them: every participant gets back whether any passed true.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool v)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred q, r;\n\t"
+        "setp.ne.u32 q, %2, 0;\n\t"
+        "bar.red.or.pred r, %1, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, r;\n\t}"
+        : "=r"(out)
+        : "r"(id), "r"(static_cast<uint32_t>(v)), "r"(count)
+        : "memory");
+    return out != 0;
 }
 
 // Address of the same shared variable in cluster CTA `rank`.

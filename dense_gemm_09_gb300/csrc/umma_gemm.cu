@@ -195,6 +195,10 @@ struct Params {
     // for 16-bit N-major B) from 32 to 256; the CTA-pair and register-path
     // kernels use 256.  The MMA is 128 x bn x UMMA_K.
     int bn;
+    // CTA-pair kernel with N-major B: the stage's B half comes as one 3-D box
+    // (column group of 128 bytes x BK rows x 128 / kNBox groups) instead of
+    // 128 / kNBox 2-D boxes
+    int b3d;
 };
 
 // The instruction descriptor with its N field (bits 17-22, N >> 3) set to n.
@@ -1052,16 +1056,30 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
 //              CTAs' loads complete on the even CTA's "full" barrier, which
 //              the even producer arms with the bytes of both halves;
 //              warps 2-5: epilogue of the CTA's 128 rows;
-//   even CTA   warp 1: the MMA issuer for the pair; it multicasts its commits
-//              to both CTAs' "empty" / "tmem_full" barriers.
+//   even CTA   warp 6: waits for each stage's "full" barrier and hands the
+//              stage to warp 1 through a named CTA barrier;
+//              warp 1: the MMA issuer for the pair (one lane issues); it
+//              multicasts its commits to both CTAs' "empty" / "tmem_full"
+//              barriers.
 // The epilogue warps of both CTAs release an accumulator by arriving on the
 // even CTA's "tmem_empty" barrier (8 warp arrivals).
+//
+// Why a separate waiter: measured on GB300, an mbarrier probe (or any
+// shared-memory access) that the MMA-issuing thread makes between one
+// stage's MMAs and the next costs ~25 % of tensor throughput at 256 x 256
+// tiles -- the thread cannot issue the next stage until the probe returns,
+// and the tensor pipe runs dry meanwhile.  A named barrier (bar.red) does not
+// have that cost: with the waits moved to warp 6, the MMA warp keeps the pipe
+// at ~97 % of its peak when the operands are already in shared memory.
 
 constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_BM = 2 * BM;                    // rows per pair tile
 constexpr int PAIR_HALF_BYTES = 128 * ROW_BYTES;   // 16 KB: 128 rows of A or of B
 constexpr int PAIR_STAGE_BYTES = 2 * PAIR_HALF_BYTES;
-constexpr int PAIR_THREADS = 192;
+constexpr int PAIR_THREADS = 224;
+constexpr int PAIR_MMA_WARP = 1;
+constexpr int PAIR_WAITER_WARP = 6;
+constexpr uint32_t PAIR_HANDOFF_THREADS = 64;  // warps 1 and 6 on named barriers 1..PAIR_STAGES
 
 struct PairCtrl {
     uint64_t full[PAIR_STAGES];   // even CTA: both halves of the stage landed
@@ -1112,6 +1130,10 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
             const int64_t nb = n0 + rank * 128;  // this CTA's half of B
             if constexpr (!T::kBNMajor) {
                 ptx::tma_load_2d_pair(sb, tmap_b, full, kc, static_cast<int32_t>(nb));
+            } else if (p.b3d) {
+                // one instruction instead of four (TF32) or two (16-bit NN):
+                // the producer thread's issue rate bounds the TF32 stage rate
+                ptx::tma_load_3d_pair(sb, tmap_b, full, 0, kc, static_cast<int32_t>(nb / T::kNBox));
             } else {
 #pragma unroll
                 for (int c = 0; c < 128 / T::kNBox; ++c)
@@ -1135,55 +1157,91 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
     }
 }
 
+// The even CTA's full-barrier waiter (warp 6): for every stage the pair
+// consumes, waits (bounded) for its "full" barrier, then meets the MMA warp on
+// named barrier 1 + stage.  The barrier's OR-reduction carries the abort flag
+// both ways, so each side runs through the same number of hand-offs and
+// neither can be left waiting on the other after a time-out.
 template <int kKind>
-__device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, PairCtrl *ctrl,
-                                         uint32_t tmem_base, WaitCtl *wc)
+__device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int lane, WaitCtl *wc)
 {
-    using T = Traits<kKind>;
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
-    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-    // test hook: wait on a barrier nothing arrives at, so the wait runs out
-    bool ok = !p.inject_stall || wait_bounded(ptx::smem_addr(&ctrl->never), 0, wc);
-    for (int64_t t = cluster; ok && t < num_tiles; t += clusters) {
-        if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u,
-                                  wc)) {
-            ok = false;
-            break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+    uint32_t stage = 0, phase = 0;
+    bool abort = false;
+    for (int64_t t = cluster; t < num_tiles; t += clusters) {
         for (int64_t kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->full[stage]), phase, wc)) {
-                ok = false;
-                break;
+            if (!abort) {
+                bool ok = true;
+                if (lane == 0) ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->full[stage]), phase, wc);
+                abort = __shfl_sync(0xffffffffu, ok ? 0 : 1, 0) != 0;
             }
-            ptx::tc_fence_after();
-            const uint32_t sa = smem_base + stage * PAIR_STAGE_BYTES;
-            const uint32_t sb = sa + PAIR_HALF_BYTES;
-#pragma unroll
-            for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
-                const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
-                uint64_t db;
-                if constexpr (!T::kBNMajor)
-                    db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
-                else
-                    db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
-                ptx::umma_pair<kKind>(d_tmem, da, db, pair_idesc<kKind>(), (kb | k) != 0 ? 1u : 0u);
-            }
-            ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), 0x3);
+            abort = ptx::bar_red_or(1 + stage, PAIR_HANDOFF_THREADS, abort);
             if (++stage == PAIR_STAGES) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
-        if (!ok) break;
-        ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->tmem_full[acc]), 0x3);
+    }
+}
+
+// The pair's MMA warp (warp 1 of the even CTA; lane 0 issues).  Per stage it
+// takes the hand-off from the waiter, issues the stage's MMAs and commits the
+// stage's release to both CTAs' "empty" barriers; per tile it waits for a free
+// accumulator and commits "tmem_full".
+template <int kKind>
+__device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, PairCtrl *ctrl,
+                                         uint32_t tmem_base, int lane, WaitCtl *wc)
+{
+    using T = Traits<kKind>;
+    const int64_t num_tiles = p.tiles_m * p.tiles_n;
+    const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    uint32_t stage = 0, acc = 0, acc_phase = 0;
+    // test hook: wait on a barrier nothing arrives at, so the wait runs out
+    bool ok = true;
+    if (lane == 0 && p.inject_stall) ok = wait_bounded(ptx::smem_addr(&ctrl->never), 0, wc);
+    bool abort = __shfl_sync(0xffffffffu, ok ? 0 : 1, 0) != 0;
+    for (int64_t t = cluster; t < num_tiles; t += clusters) {
+        if (!abort) {
+            ok = true;
+            if (lane == 0)
+                ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u, wc);
+            abort = __shfl_sync(0xffffffffu, ok ? 0 : 1, 0) != 0;
+        }
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+            abort = ptx::bar_red_or(1 + stage, PAIR_HANDOFF_THREADS, abort);
+            if (!abort) {
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sa = smem_base + stage * PAIR_STAGE_BYTES;
+                    const uint32_t sb = sa + PAIR_HALF_BYTES;
+#pragma unroll
+                    for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
+                        const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
+                        uint64_t db;
+                        if constexpr (!T::kBNMajor)
+                            db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
+                        else
+                            db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
+                        ptx::umma_pair<kKind>(d_tmem, da, db, pair_idesc<kKind>(), (kb | k) != 0 ? 1u : 0u);
+                    }
+                    ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), 0x3);
+                }
+                __syncwarp();
+            }
+            if (++stage == PAIR_STAGES) stage = 0;
+        }
+        if (!abort && lane == 0) ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->tmem_full[acc]), 0x3);
+        __syncwarp();
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
     }
-    ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->mma_done), 0x1);
-    drain_wait(ptx::smem_addr(&ctrl->mma_done), 0);
+    if (lane == 0) {
+        ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->mma_done), 0x1);
+        drain_wait(ptx::smem_addr(&ctrl->mma_done), 0);
+    }
+    __syncwarp();
 }
 
 template <int kKind>
@@ -1261,8 +1319,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) pair_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
-    } else if (warp == 1) {
-        if (lane == 0 && rank == 0) pair_mma<kKind>(p, smem_base, ctrl, tmem_base, wc);
+    } else if (warp == PAIR_MMA_WARP) {
+        if (rank == 0) pair_mma<kKind>(p, smem_base, ctrl, tmem_base, lane, wc);
+    } else if (warp == PAIR_WAITER_WARP) {
+        if (rank == 0) pair_waiter<kKind>(p, ctrl, lane, wc);
     } else {
         pair_epilogue<kKind>(p, &tmap_c, ctrl, tmem_base, smem_base + PAIR_STAGES * PAIR_STAGE_BYTES,
                              rank, warp, lane, wc);
@@ -1310,6 +1370,21 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A 3-D tiled map (dims innermost first; byte strides of dims 1 and 2), 128-
+// byte swizzle family, zero fill out of range.
+bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, const uint64_t (&dims)[3],
+                 const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    cuuint64_t st[2] = {strides[0], strides[1]};
+    cuuint32_t b[3] = {box[0], box[1], box[2]};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void *>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int kKind, bool kTma>
@@ -1398,6 +1473,7 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, 
     Params p;
     p.bn = BN;
     p.tma_store = 0;
+    p.b3d = 0;
     p.inject_stall = t_inject_limit_ns ? 1 : 0;
     p.splitk = 1;
     p.wait_limit_ns = t_inject_limit_ns ? t_inject_limit_ns : kWaitLimitNs;
@@ -1664,7 +1740,26 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
         };
         CUtensorMap probe{};
         if (make_b(BN, &probe)) {
-            const bool ok_pair = make_b(128, &mbp);
+            bool ok_pair = make_b(128, &mbp);
+            if constexpr (T::kBNMajor) {
+                // B viewed as [N / kNBox column groups][K rows][kNBox columns]:
+                // one box holds the pair CTA's 128 columns of a stage, in the
+                // same shared-memory layout as 128 / kNBox separate 2-D boxes.
+                // Only when N is a whole number of groups: a partial last
+                // group would read past the end of B's rows.
+                CUtensorMap m3{};
+                if (ok_pair && N % T::kNBox == 0 &&
+                    make_map_3d(&m3, dt, B,
+                                {static_cast<uint64_t>(T::kNBox), static_cast<uint64_t>(K),
+                                 static_cast<uint64_t>(N / T::kNBox)},
+                                {static_cast<uint64_t>(ldb * es), static_cast<uint64_t>(T::kNBox * es)},
+                                {static_cast<uint32_t>(T::kNBox), static_cast<uint32_t>(T::BK),
+                                 static_cast<uint32_t>(128 / T::kNBox)},
+                                T::kTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)) {
+                    mbp = m3;
+                    p.b3d = 1;
+                }
+            }
             return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, make_b, mc, stream, dev);
         }
     }

@@ -270,6 +270,23 @@ def test_pair_kernel_m_tails(path, M):
     assert parity.worst_ratio(path, got, A, B, C, 1.5, -0.25) <= 1.0
 
 
+@pytest.mark.parametrize("path", ["tf32", "f16_nn", "bf16_nn"])
+@pytest.mark.parametrize("N", [256, 320, 544, 576, 1000, 1024])
+def test_pair_kernel_n_major_b(path, N):
+    import dense_gemm_09_gb300 as dg
+    # N-major B in the pair kernel: when N is a whole number of 128-byte
+    # column groups (32 TF32 or 64 16-bit columns) a stage's B half is one
+    # 3-D box, otherwise 128-byte 2-D boxes; N past the last pair tile's
+    # first half (320, 544, 576, 1000) leaves the odd CTA's columns partly or
+    # wholly outside B.
+    M, K = 300, 520
+    A, B, C = parity.host_operands(path, M, N, K, seed=N)
+    dg.tune_next(dg.TUNE_PAIR)
+    got, _, _ = parity.run(path, A, B, C, 0.75, 0.5)
+    assert "_pair_" in dg.last_kernel()
+    assert parity.worst_ratio(path, got, A, B, C, 0.75, 0.5) <= 1.0
+
+
 # Few output tiles and a long K: the split-K kernel (a cluster of S CTAs per
 # tile, partials reduced in distributed shared memory).
 SPLITK_CASES = [
