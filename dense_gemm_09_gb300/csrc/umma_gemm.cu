@@ -330,6 +330,9 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
             ptx::tma_load_2d(sa, tmap_a, full, kc, static_cast<int32_t>(m0));
             if constexpr (!T::kBNMajor) {
                 ptx::tma_load_2d(sb, tmap_b, full, kc, static_cast<int32_t>(n0));
+            } else if (p.b3d) {
+                // B is N-major, all bn / kNBox column groups in one 3-D box
+                ptx::tma_load_3d(sb, tmap_b, full, 0, kc, static_cast<int32_t>(n0 / T::kNBox));
             } else {
                 // B is N-major: boxes of 128 bytes of columns x BK rows, one
                 // swizzle column each (see Traits)
@@ -1562,10 +1565,9 @@ constexpr int bn_step()
     return Traits<kKind>::kBNMajor ? Traits<kKind>::kNBox : 32;
 }
 
-// Automatic choice.  Problems with more than one wave of 128 x 256 tiles
-// take the pair kernel (M > 128); between half a wave and one wave, the
-// single-CTA kernel with 256-wide tiles.  Smaller ones -- skinny M, or few
-// tiles and a long K -- choose the
+// Automatic choice.  Problems with more than half a wave of 128 x 256 tiles
+// take the pair kernel (M > 128; else the single-CTA kernel, 256 wide).
+// Smaller ones -- skinny M, or few tiles and a long K -- choose the
 // tile width bn and the split S that keep the most SMs streaming:
 //   * candidates: bn from 256 down in the kind's step (32, or 64 for the
 //     16-bit NN kinds); S from 1 to 8 with at least 8 K blocks per rank,
@@ -1584,11 +1586,10 @@ UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok)
 {
     using T = Traits<kKind>;
     const int64_t tiles256 = p.tiles_m * ((p.N + BN - 1) / BN);
-    // more than one wave of 128 x 256 tiles: the pair halves each CTA's
-    // operand traffic; within one wave the single-CTA kernel is as fast and
-    // has less to synchronise (2048^3 FP16: 21.2 us single, 22.9 us pair)
-    if (tiles256 > sm_count) return {pair_ok && p.M > BM ? kVariantPair : kVariantSingle, BN, 1};
-    if (tiles256 * 2 > sm_count) return {kVariantSingle, BN, 1};
+    // more than half a wave of 128 x 256 tiles: the pair halves each CTA's
+    // operand traffic (2048^3: FP16 21.3 us pair, 22.0 us single; TF32 31.4
+    // and 34.6 us)
+    if (tiles256 * 2 > sm_count) return {pair_ok && p.M > BM ? kVariantPair : kVariantSingle, BN, 1};
     const double kb_mma_us = 0.33 / 256.0;          // per column of bn, one K block
     const double sm_bytes_per_us = 75e3;            // 75 GB/s
     const double hbm_bytes_per_us = 6.0e6;          // 6 TB/s
@@ -1674,7 +1675,7 @@ const char *variant_name(int variant, int bn = BN, int split = 1)
 // pair kernel (null if B cannot be described); make_b(bn, map) builds B's map
 // for 128 x bn tiles.
 template <int kKind, typename MakeB>
-const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *mb_pair,
+const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *mb_pair, int pair3d,
                          MakeB make_b, const CUtensorMap &mc, cudaStream_t stream, const DeviceInfo &dev)
 {
     UmmaConfig cfg = t_tune;
@@ -1689,6 +1690,7 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
     Params p = p0;
     if (cfg.variant == kVariantPair) {
         p.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
+        p.b3d = pair3d;
         if (launch_pair<kKind>(ma, *mb_pair, mc, p, stream)) return variant_name<kKind>(kVariantPair);
         cfg = UmmaConfig{kVariantSingle, BN, 1};
         p = p0;
@@ -1697,7 +1699,9 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
     p.tiles_n = (p.N + cfg.bn - 1) / cfg.bn;
     if (p.bn % box_cols<kKind>() != 0) p.tma_store = 0;
     CUtensorMap mb{};
-    if (!make_b(cfg.bn, &mb)) return nullptr;
+    int b3d = 0;
+    if (!make_b(cfg.bn, &mb, &b3d)) return nullptr;
+    p.b3d = b3d;
     if (cfg.variant == kVariantSplit) {
         p.splitk = cfg.split;
         if (launch_splitk<kKind>(ma, mb, mc, p, stream))
@@ -1728,39 +1732,39 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
     const bool tma = aligned16(A) && aligned16(B) && (lda * es) % 16 == 0 && (ldb * es) % 16 == 0;
     CUtensorMap ma{}, mbp{};
     if (tma && make_map(&ma, dt, A, K, M, lda * es, T::BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) {
-        // B stored K x N: boxes of 128 bytes of columns x BK rows, whatever the
-        // tile width; B stored N x K: bn-row boxes (single CTA), 128-row boxes
-        // (pair)
-        auto make_b = [&](int bn, CUtensorMap *m) {
-            if constexpr (T::kBNMajor)
-                return make_map(m, dt, B, N, K, ldb * es, T::kNBox, T::BK,
-                                T::kTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
-            else
-                return make_map(m, dt, B, K, N, ldb * es, T::BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
-        };
-        CUtensorMap probe{};
-        if (make_b(BN, &probe)) {
-            bool ok_pair = make_b(128, &mbp);
+        // B stored N x K: bn-row boxes (single CTA), 128-row boxes (pair).
+        // B stored K x N (N-major): when N is a whole number of 128-byte
+        // column groups, one 3-D box per stage -- B viewed as [N / kNBox
+        // groups][K rows][kNBox columns], a box of bn / kNBox groups -- which
+        // lands in the same shared-memory layout as bn / kNBox 2-D boxes of 128
+        // bytes x BK rows, in one instruction; otherwise the 2-D boxes (a
+        // partial last group would read past the end of B's rows).
+        auto make_b = [&](int bn, CUtensorMap *m, int *b3d) {
+            *b3d = 0;
             if constexpr (T::kBNMajor) {
-                // B viewed as [N / kNBox column groups][K rows][kNBox columns]:
-                // one box holds the pair CTA's 128 columns of a stage, in the
-                // same shared-memory layout as 128 / kNBox separate 2-D boxes.
-                // Only when N is a whole number of groups: a partial last
-                // group would read past the end of B's rows.
-                CUtensorMap m3{};
-                if (ok_pair && N % T::kNBox == 0 &&
-                    make_map_3d(&m3, dt, B,
+                const CUtensorMapSwizzle sw =
+                    T::kTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+                if (N % T::kNBox == 0 &&
+                    make_map_3d(m, dt, B,
                                 {static_cast<uint64_t>(T::kNBox), static_cast<uint64_t>(K),
                                  static_cast<uint64_t>(N / T::kNBox)},
                                 {static_cast<uint64_t>(ldb * es), static_cast<uint64_t>(T::kNBox * es)},
                                 {static_cast<uint32_t>(T::kNBox), static_cast<uint32_t>(T::BK),
-                                 static_cast<uint32_t>(128 / T::kNBox)},
-                                T::kTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)) {
-                    mbp = m3;
-                    p.b3d = 1;
+                                 static_cast<uint32_t>(bn / T::kNBox)},
+                                sw)) {
+                    *b3d = 1;
+                    return true;
                 }
+                return make_map(m, dt, B, N, K, ldb * es, T::kNBox, T::BK, sw);
+            } else {
+                return make_map(m, dt, B, K, N, ldb * es, T::BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
             }
-            return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, make_b, mc, stream, dev);
+        };
+        CUtensorMap probe{};
+        int probe3d = 0, pair3d = 0;
+        if (make_b(BN, &probe, &probe3d)) {
+            const bool ok_pair = make_b(128, &mbp, &pair3d);
+            return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, pair3d, make_b, mc, stream, dev);
         }
     }
     t_tune = UmmaConfig{kVariantAuto, BN, 1};

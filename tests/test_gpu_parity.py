@@ -250,7 +250,12 @@ def test_kernel_variant_names(path):
         got, _, _ = parity.run(path, A, B, C, 1.0, 0.0)
         assert dg.last_kernel().endswith("_tma") and "_pair_" in dg.last_kernel()
         assert parity.worst_ratio(path, got, A, B, C, 1.0, 0.0) <= 1.0
-        # half a wave to one wave of tiles: the single-CTA kernel, 256 wide
+        # half a wave to one wave of tiles: the pair too when M > 128 ...
+        A, B, C = parity.host_operands(path, 2048, 2048, 64, seed=1)
+        got, _, _ = parity.run(path, A, B, C, 1.0, 0.0)
+        assert dg.last_kernel().endswith("_tma") and "_pair_" in dg.last_kernel()
+        assert parity.worst_ratio(path, got, A, B, C, 1.0, 0.0) <= 1.0
+        # ... and the single-CTA kernel, 256 wide, for a single row band
         A, B, C = parity.host_operands(path, 128, 20480, 64, seed=1)
         got, _, _ = parity.run(path, A, B, C, 1.0, 0.0)
         assert "_128x256x" in dg.last_kernel() and dg.last_kernel().endswith("_tma")
