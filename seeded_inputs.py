@@ -78,6 +78,12 @@ def small_integers(shape, g: torch.Generator, bound: int = 4, dtype=torch.float3
     return torch.randint(-bound, bound + 1, shape, generator=g).to(dtype)
 
 
+def small_integers_i8(shape, g: torch.Generator, bound: int = 1) -> torch.Tensor:
+    """Integers in [-bound, bound] as int8 (one byte each: operands of more
+    than 2^31 elements stay a few GB on the host)."""
+    return torch.randint(-bound, bound + 1, shape, generator=g, dtype=torch.int8)
+
+
 def make(w: Workload, seed: int | None = None, pin: bool = False):
     """Host operands (A, B, C) for workload ``w``.
 
