@@ -1104,33 +1104,58 @@ constexpr uint32_t pair_idesc()
     return (Traits<kKind>::kIdesc & ~(0x1Fu << 24)) | (static_cast<uint32_t>(PAIR_BM >> 4) << 24);
 }
 
-template <int kKind>
+// Clusters of kPairs CTA pairs (2 * kPairs CTAs; the pair of rank r is r / 2,
+// its leader the even CTA 2 * (r / 2)).  With kPairs = 2 the two pairs take
+// side-by-side output tiles of the same 256 rows -- a 256 x 512 supertile --
+// and share its A band: each CTA loads 64 of its half's 128 rows and
+// multicasts them to the same half of both pairs, so a CTA reads 24 KB per
+// stage from L2 instead of 32 KB.  The stage ring of every CTA is then
+// written by both pairs' producers, so each "empty" barrier counts one
+// commit from each pair's MMA warp.
+template <int kPairs>
+__device__ __forceinline__ void pair_tile(int64_t t, const Params &p, uint32_t rank, int64_t &m0,
+                                          int64_t &n0)
+{
+    tile_coords(t, p, m0, n0, PAIR_BM);  // n0: supertile column x BN
+    n0 = n0 * kPairs + static_cast<int64_t>(rank >> 1) * BN;
+}
+
+template <int kKind, int kPairs>
 __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
                                               const Params &p, uint32_t smem_base, PairCtrl *ctrl,
                                               uint32_t rank, WaitCtl *wc)
 {
     using T = Traits<kKind>;
+    constexpr int kCtas = 2 * kPairs;
+    constexpr int kRowsA = 128 / kPairs;  // A rows this CTA loads per stage
+    constexpr uint16_t kHalfMask = kPairs == 1 ? 0x1 : 0x5;  // the even CTA of every pair
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
-    const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const int64_t cluster = blockIdx.x / kCtas, clusters = gridDim.x / kCtas;
+    const uint32_t half = rank & 1u, pair = rank >> 1, leader = rank & ~1u;
     uint32_t stage = 0, phase = 0;
     uint32_t issued = 0, issued_phase = 0;
     bool ok = true;
     for (int64_t t = cluster; ok && t < num_tiles; t += clusters) {
         int64_t m0, n0;
-        tile_coords(t, p, m0, n0, PAIR_BM);
+        pair_tile<kPairs>(t, p, rank, m0, n0);
         for (int64_t kb = 0; kb < p.num_kb; ++kb) {
             if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
                 ok = false;
                 break;
             }
             const uint32_t full_local = ptx::smem_addr(&ctrl->full[stage]);
-            const uint32_t full = ptx::mapa(full_local, 0);  // the even CTA's barrier
-            if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, 2 * PAIR_STAGE_BYTES);
+            const uint32_t full = ptx::mapa(full_local, leader);  // the pair leader's barrier
+            if (half == 0) ptx::mbar_arrive_expect_tx(full_local, 2 * PAIR_STAGE_BYTES);
             const uint32_t sa = smem_base + stage * PAIR_STAGE_BYTES;
             const uint32_t sb = sa + PAIR_HALF_BYTES;
             const int32_t kc = static_cast<int32_t>(kb * T::BK);
-            ptx::tma_load_2d_pair(sa, tmap_a, full, kc, static_cast<int32_t>(m0 + rank * 128));
-            const int64_t nb = n0 + rank * 128;  // this CTA's half of B
+            const int32_t ma = static_cast<int32_t>(m0 + half * 128 + pair * kRowsA);
+            if constexpr (kPairs == 1)
+                ptx::tma_load_2d_pair(sa, tmap_a, full, kc, ma);
+            else
+                ptx::tma_load_2d_pair_multicast(sa + pair * kRowsA * ROW_BYTES, tmap_a, full, kc, ma,
+                                                static_cast<uint16_t>(kHalfMask << half));
+            const int64_t nb = n0 + half * 128;  // this CTA's half of B
             if constexpr (!T::kBNMajor) {
                 ptx::tma_load_2d_pair(sb, tmap_b, full, kc, static_cast<int32_t>(nb));
             } else if (p.b3d) {
@@ -1151,8 +1176,8 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
             }
         }
     }
-    if (!ok && rank == 0) {
-        // The even CTA's barrier counts both CTAs' bytes: wait (bounded) for
+    if (!ok && half == 0) {
+        // The leader's barrier counts both CTAs' bytes: wait (bounded) for
         // the loads in flight before the pair leaves.
         for (int s = 0; s < PAIR_STAGES; ++s)
             if ((issued >> s) & 1u)
@@ -1160,16 +1185,16 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
     }
 }
 
-// The even CTA's full-barrier waiter (warp 6): for every stage the pair
+// A pair leader's full-barrier waiter (warp 6): for every stage the pair
 // consumes, waits (bounded) for its "full" barrier, then meets the MMA warp on
 // named barrier 1 + stage.  The barrier's OR-reduction carries the abort flag
 // both ways, so each side runs through the same number of hand-offs and
 // neither can be left waiting on the other after a time-out.
-template <int kKind>
+template <int kKind, int kPairs>
 __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int lane, WaitCtl *wc)
 {
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
-    const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
     uint32_t stage = 0, phase = 0;
     bool abort = false;
     for (int64_t t = cluster; t < num_tiles; t += clusters) {
@@ -1188,17 +1213,20 @@ __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int
     }
 }
 
-// The pair's MMA warp (warp 1 of the even CTA; lane 0 issues).  Per stage it
+// A pair's MMA warp (warp 1 of the leader; lane 0 issues).  Per stage it
 // takes the hand-off from the waiter, issues the stage's MMAs and commits the
-// stage's release to both CTAs' "empty" barriers; per tile it waits for a free
-// accumulator and commits "tmem_full".
-template <int kKind>
+// stage's release to the "empty" barriers of every CTA of the cluster (with
+// two pairs, both pairs' producers write each CTA's ring); per tile it waits
+// for a free accumulator and commits "tmem_full" to its own pair.
+template <int kKind, int kPairs>
 __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, PairCtrl *ctrl,
-                                         uint32_t tmem_base, int lane, WaitCtl *wc)
+                                         uint32_t tmem_base, uint32_t rank, int lane, WaitCtl *wc)
 {
     using T = Traits<kKind>;
+    constexpr uint16_t kAll = static_cast<uint16_t>((1u << (2 * kPairs)) - 1u);
+    const uint16_t kPair = static_cast<uint16_t>(0x3u << rank);
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
-    const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
     uint32_t stage = 0, acc = 0, acc_phase = 0;
     // test hook: wait on a barrier nothing arrives at, so the wait runs out
     bool ok = true;
@@ -1229,54 +1257,55 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
                             db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
                         ptx::umma_pair<kKind>(d_tmem, da, db, pair_idesc<kKind>(), (kb | k) != 0 ? 1u : 0u);
                     }
-                    ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), 0x3);
+                    ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), kAll);
                 }
                 __syncwarp();
             }
             if (++stage == PAIR_STAGES) stage = 0;
         }
-        if (!abort && lane == 0) ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->tmem_full[acc]), 0x3);
+        if (!abort && lane == 0) ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->tmem_full[acc]), kPair);
         __syncwarp();
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
     }
     if (lane == 0) {
-        ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->mma_done), 0x1);
+        ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->mma_done), static_cast<uint16_t>(1u << rank));
         drain_wait(ptx::smem_addr(&ctrl->mma_done), 0);
     }
     __syncwarp();
 }
 
-template <int kKind>
+template <int kKind, int kPairs>
 __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap *tmap_c,
                                               PairCtrl *ctrl, uint32_t tmem_base, uint32_t epi_smem,
                                               uint32_t rank, int warp, int lane, WaitCtl *wc)
 {
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
-    const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
     const uint32_t quarter = static_cast<uint32_t>(warp & 3);
+    const uint32_t leader = rank & ~1u;
     uint32_t acc = 0, acc_phase = 0, nbox = 0;
     for (int64_t t = cluster; t < num_tiles; t += clusters) {
         int64_t m0, n0;
-        tile_coords(t, p, m0, n0, PAIR_BM);
+        pair_tile<kPairs>(t, p, rank, m0, n0);
         bool ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * BN;
-        drain_rows<kKind>(p, tmap_c, taddr, m0 + rank * 128 + quarter * 32, n0,
+        drain_rows<kKind>(p, tmap_c, taddr, m0 + (rank & 1u) * 128 + quarter * 32, n0,
                           epi_smem + quarter * 2 * EPI_BOX_BYTES, lane, nbox);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0)
-            ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_addr(&ctrl->tmem_empty[acc]), 0));
+            ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_addr(&ctrl->tmem_empty[acc]), leader));
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
     }
     if (lane == 0) ptx::bulk_wait<0>();  // stores done before the CTA leaves
 }
 
-template <int kKind>
+template <int kKind, int kPairs>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     umma_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
@@ -1288,11 +1317,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     PairCtrl *ctrl = reinterpret_cast<PairCtrl *>(smem + PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ptx::cluster_ctarank();
+    const bool leader = (rank & 1u) == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < PAIR_STAGES; ++s) {
             ptx::mbar_init(ptx::smem_addr(&ctrl->full[s]), 1);
-            ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), kPairs);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_full[a]), 1);
@@ -1309,32 +1339,32 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         ptx::prefetch_tmap(&tmap_b);
     }
     if (p.tma_store && warp == 2 && lane == 0) ptx::prefetch_tmap(&tmap_c);
-    if (warp == 1) {
+    if (warp == PAIR_MMA_WARP) {
         ptx::tmem_alloc_pair(ptx::smem_addr(&ctrl->tmem_base), TMEM_COLS);
         ptx::tmem_relinquish_pair();
     }
     ptx::tc_fence_before();
-    ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    ptx::cluster_sync();  // every CTA's barriers exist before any cross-CTA signal
     ptx::tc_fence_after();
     const uint32_t tmem_base = ctrl->tmem_base;
     WaitCtl *wc = &ctrl->wait;
     const uint32_t smem_base = ptx::smem_addr(smem);
 
     if (warp == 0) {
-        if (lane == 0) pair_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
+        if (lane == 0) pair_producer<kKind, kPairs>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
     } else if (warp == PAIR_MMA_WARP) {
-        if (rank == 0) pair_mma<kKind>(p, smem_base, ctrl, tmem_base, lane, wc);
+        if (leader) pair_mma<kKind, kPairs>(p, smem_base, ctrl, tmem_base, rank, lane, wc);
     } else if (warp == PAIR_WAITER_WARP) {
-        if (rank == 0) pair_waiter<kKind>(p, ctrl, lane, wc);
+        if (leader) pair_waiter<kKind, kPairs>(p, ctrl, lane, wc);
     } else {
-        pair_epilogue<kKind>(p, &tmap_c, ctrl, tmem_base, smem_base + PAIR_STAGES * PAIR_STAGE_BYTES,
-                             rank, warp, lane, wc);
+        pair_epilogue<kKind, kPairs>(p, &tmap_c, ctrl, tmem_base, smem_base + PAIR_STAGES * PAIR_STAGE_BYTES,
+                                     rank, warp, lane, wc);
     }
 
     __syncwarp();  // the barrier below is warp-aligned: reconverge lane 0 with the rest
     ptx::tc_fence_before();
-    ptx::cluster_sync();  // no CTA leaves while its partner may still signal it
-    if (warp == 1) {
+    ptx::cluster_sync();  // no CTA leaves while another may still signal or write it
+    if (warp == PAIR_MMA_WARP) {
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
@@ -1404,9 +1434,9 @@ bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
     return true;
 }
 
-// Co-resident clusters of the pair kernel on the current device (0 if the
-// pair kernel cannot run), cached per device and operand kind.
-template <int kKind>
+// Co-resident clusters of the pair kernel (clusters of 2 * kPairs CTAs) on the
+// current device (0 if the kernel cannot run), cached per device and kind.
+template <int kKind, int kPairs>
 int pair_clusters()
 {
     constexpr int kMaxDevices = 64;
@@ -1416,22 +1446,22 @@ int pair_clusters()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     std::call_once(once[dev], [dev] {
         int n = 0;
-        if (cudaFuncSetAttribute(umma_pair_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(umma_pair_kernel<kKind, kPairs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PAIR_SMEM_BYTES) == cudaSuccess) {
             int sms = 0;
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.x = 2 * kPairs;
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+            cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % (2 * kPairs)));
             cfg.blockDim = dim3(PAIR_THREADS);
             cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, umma_pair_kernel<kKind>, &cfg) != cudaSuccess) n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, umma_pair_kernel<kKind, kPairs>, &cfg) != cudaSuccess) n = 0;
         }
         cudaGetLastError();  // a failed query leaves no sticky error behind
         cached[dev] = n;
@@ -1439,27 +1469,29 @@ int pair_clusters()
     return cached[dev];
 }
 
-template <int kKind>
+// p.tiles_m / p.tiles_n count 256-row bands and supertile columns (256 * kPairs
+// columns each).
+template <int kKind, int kPairs>
 bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const Params &p,
                  cudaStream_t stream)
 {
-    const int clusters = pair_clusters<kKind>();
+    const int clusters = pair_clusters<kKind, kPairs>();
     if (clusters <= 0) return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
     const int64_t n = tiles < clusters ? tiles : clusters;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = 2 * kPairs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * kPairs * n));
     cfg.blockDim = dim3(PAIR_THREADS);
     cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind>, ma, mb, mc, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kPairs>, ma, mb, mc, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -1547,7 +1579,7 @@ int cluster_capacity(int size)
 // Tile configuration of one call: the CTA-pair kernel (256 x 256 tiles), the
 // persistent single-CTA kernel (128 x bn tiles) or split-K over S CTAs of a
 // cluster (128 x bn tiles).
-enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3 };
+enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3, kVariantQuad = 4 };
 struct UmmaConfig {
     int variant;
     int bn;
@@ -1582,13 +1614,18 @@ constexpr int bn_step()
 // ~0.33 us, a CTA streams ~75 GB/s, HBM ~6 TB/s; a split costs ~1 us plus
 // ~0.5 us per extra rank plus ~0.9 us per 64 KB of partials moved.
 template <int kKind>
-UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok)
+UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok, bool x2_ok)
 {
     using T = Traits<kKind>;
     const int64_t tiles256 = p.tiles_m * ((p.N + BN - 1) / BN);
     // more than half a wave of 128 x 256 tiles: the pair halves each CTA's
     // operand traffic (2048^3: FP16 21.3 us pair, 22.0 us single; TF32 31.4
     // and 34.6 us)
+    // (two pairs per cluster sharing A -- x2_ok -- measured slower at 8192 x
+    // 8192 x 4096: TF32 901 vs 994 TFLOP/s, FP16 1755 vs 1778; each SM still
+    // receives 32 KB per stage, and the shared ring couples the two pairs.
+    // It stays reachable through dgemm_tune_next.)
+    (void)x2_ok;
     if (tiles256 * 2 > sm_count) return {pair_ok && p.M > BM ? kVariantPair : kVariantSingle, BN, 1};
     const double kb_mma_us = 0.33 / 256.0;          // per column of bn, one K block
     const double sm_bytes_per_us = 75e3;            // 75 GB/s
@@ -1648,7 +1685,7 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorM
 template <int kKind>
 const char *variant_name(int variant, int bn = BN, int split = 1)
 {
-    static std::string names[2 + 9 * 9];
+    static std::string names[3 + 9 * 9];
     static std::once_flag once;
     std::call_once(once, [] {
         using T = Traits<kKind>;
@@ -1657,6 +1694,7 @@ const char *variant_name(int variant, int bn = BN, int split = 1)
         const std::string bk = std::to_string(T::BK);
         const std::string base = std::string("umma_") + kind;
         names[0] = base + "_pair_256x256x" + bk + "_tma";
+        names[2 + 9 * 9] = base + "_pair_x2_256x512x" + bk + "_tma";
         names[1] = base + "_128x256x" + bk + (kKind == kTF32 ? "_cpasync" : "_ldst");
         for (int w = 1; w <= 8; ++w) {
             const std::string tile = "128x" + std::to_string(32 * w) + "x" + bk;
@@ -1666,6 +1704,7 @@ const char *variant_name(int variant, int bn = BN, int split = 1)
         }
     });
     if (variant == kVariantPair) return names[0].c_str();
+    if (variant == kVariantQuad) return names[2 + 9 * 9].c_str();
     if (variant == kVariantAuto) return names[1].c_str();  // the non-TMA kernel
     const int w = bn / 32, S = variant == kVariantSplit ? split : 1;
     return names[2 + w * 9 + S].c_str();
@@ -1675,23 +1714,32 @@ const char *variant_name(int variant, int bn = BN, int split = 1)
 // pair kernel (null if B cannot be described); make_b(bn, map) builds B's map
 // for 128 x bn tiles.
 template <int kKind, typename MakeB>
-const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *mb_pair, int pair3d,
-                         MakeB make_b, const CUtensorMap &mc, cudaStream_t stream, const DeviceInfo &dev)
+const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *ma_x2,
+                         const CUtensorMap *mb_pair, int pair3d, MakeB make_b, const CUtensorMap &mc,
+                         cudaStream_t stream, const DeviceInfo &dev)
 {
     UmmaConfig cfg = t_tune;
     t_tune = UmmaConfig{kVariantAuto, BN, 1};
-    if ((cfg.variant == kVariantPair && !mb_pair) || cfg.bn % bn_step<kKind>() != 0)
+    if (((cfg.variant == kVariantPair || cfg.variant == kVariantQuad) && !mb_pair) ||
+        cfg.bn % bn_step<kKind>() != 0)
         cfg.variant = kVariantAuto;
+    if (cfg.variant == kVariantQuad && !ma_x2) cfg.variant = kVariantPair;
     // every rank of a split needs at least one K block
     if (cfg.variant == kVariantSplit && cfg.split > p0.num_kb)
         cfg = p0.num_kb >= 2 ? UmmaConfig{kVariantSplit, cfg.bn, static_cast<int>(p0.num_kb)}
                              : UmmaConfig{kVariantSingle, cfg.bn, 1};
-    if (cfg.variant == kVariantAuto) cfg = choose_config<kKind>(p0, dev.sm_count, mb_pair != nullptr);
+    if (cfg.variant == kVariantAuto)
+        cfg = choose_config<kKind>(p0, dev.sm_count, mb_pair != nullptr, ma_x2 != nullptr);
     Params p = p0;
-    if (cfg.variant == kVariantPair) {
+    if (cfg.variant == kVariantPair || cfg.variant == kVariantQuad) {
         p.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
         p.b3d = pair3d;
-        if (launch_pair<kKind>(ma, *mb_pair, mc, p, stream)) return variant_name<kKind>(kVariantPair);
+        if (cfg.variant == kVariantQuad) {
+            Params q = p;
+            q.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);  // 256 x 512 supertiles
+            if (launch_pair<kKind, 2>(*ma_x2, *mb_pair, mc, q, stream)) return variant_name<kKind>(kVariantQuad);
+        }
+        if (launch_pair<kKind, 1>(ma, *mb_pair, mc, p, stream)) return variant_name<kKind>(kVariantPair);
         cfg = UmmaConfig{kVariantSingle, BN, 1};
         p = p0;
     }
@@ -1764,7 +1812,11 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
         int probe3d = 0, pair3d = 0;
         if (make_b(BN, &probe, &probe3d)) {
             const bool ok_pair = make_b(128, &mbp, &pair3d);
-            return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, pair3d, make_b, mc, stream, dev);
+            // two pairs per cluster: each CTA loads 64 of its half's A rows
+            CUtensorMap ma_x2{};
+            const bool ok_x2 = make_map(&ma_x2, dt, A, K, M, lda * es, T::BK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+            return dispatch_tma<kKind>(p, ma, ok_x2 ? &ma_x2 : nullptr, ok_pair ? &mbp : nullptr, pair3d, make_b,
+                                       mc, stream, dev);
         }
     }
     t_tune = UmmaConfig{kVariantAuto, BN, 1};
@@ -1796,10 +1848,12 @@ const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, 
 
 int umma_tune_next(int variant, int bn, int split)
 {
-    if (variant < kVariantAuto || variant > kVariantSplit) return DGEMM_ERR_INVALID_ARG;
-    if (variant >= kVariantSingle && (bn < 32 || bn > BN || bn % 32 != 0)) return DGEMM_ERR_INVALID_ARG;
+    if (variant < kVariantAuto || variant > kVariantQuad) return DGEMM_ERR_INVALID_ARG;
+    if ((variant == kVariantSingle || variant == kVariantSplit) && (bn < 32 || bn > BN || bn % 32 != 0))
+        return DGEMM_ERR_INVALID_ARG;
     if (variant == kVariantSplit && (split < 2 || split > 8)) return DGEMM_ERR_INVALID_ARG;
-    t_tune = UmmaConfig{variant, variant >= kVariantSingle ? bn : BN, variant == kVariantSplit ? split : 1};
+    const bool sized = variant == kVariantSingle || variant == kVariantSplit;
+    t_tune = UmmaConfig{variant, sized ? bn : BN, variant == kVariantSplit ? split : 1};
     return DGEMM_OK;
 }
 
