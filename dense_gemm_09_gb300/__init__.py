@@ -72,6 +72,10 @@ def lib():
         L.dgemm_last_kernel.restype = ctypes.c_char_p
         L.dgemm_tune_next.argtypes = [ci, ci, ci]
         L.dgemm_tune_next.restype = ci
+        L.gemm_tf32_ws.argtypes = sig[:11] + [vp, i64, vp]
+        L.gemm_tf32_ws.restype = ci
+        L.gemm_tf32_workspace_bytes.argtypes = [i64, i64, i64, vp, i64, vp, i64]
+        L.gemm_tf32_workspace_bytes.restype = i64
         _lib = L
         return L
 
@@ -97,8 +101,8 @@ TUNE_AUTO, TUNE_PAIR, TUNE_SINGLE, TUNE_SPLIT, TUNE_PAIR_X2 = 0, 1, 2, 3, 4
 
 def tune_next(variant: int, bn: int = 256, split: int = 1) -> None:
     """Tuning hook: fix the tile configuration of the next tensor-core call
-    on this thread (variant TUNE_PAIR / TUNE_PAIR_X2 / TUNE_SINGLE / TUNE_SPLIT, tile width
-    bn, split-K factor split)."""
+    on this thread (variant TUNE_PAIR / TUNE_PAIR_X2 / TUNE_SINGLE /
+    TUNE_SPLIT, tile width bn, split-K factor split)."""
     st = lib().dgemm_tune_next(int(variant), int(bn), int(split))
     if st != OK:
         raise DgemmError(st, "dgemm_tune_next")
@@ -119,7 +123,9 @@ def _mat(t: torch.Tensor, name: str, dtype: torch.dtype):
     rows, cols = t.shape
     if cols > 1 and t.stride(1) != 1:
         raise ValueError("%s must have unit column stride" % name)
-    ld = t.stride(0) if rows > 1 else cols
+    # the row stride as stored, also for one row (it decides whether the TMA
+    # kernels can load the matrix); never below the row length
+    ld = t.stride(0) if rows > 0 else cols
     return t.data_ptr(), max(ld, cols)
 
 
@@ -156,6 +162,40 @@ def gemm_f32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
 def gemm_tf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
     """C = alpha * A @ B + beta * C with TF32 tensor-core products."""
     return _nn("gemm_tf32", A, B, C, alpha, beta, stream)
+
+
+def tf32_workspace_bytes(A, B) -> int:
+    """Bytes of workspace gemm_tf32_ws needs for these operands (0: none)."""
+    pa, lda = _mat(A, "A", torch.float32)
+    pb, ldb = _mat(B, "B", torch.float32)
+    M, K = A.shape
+    n = lib().gemm_tf32_workspace_bytes(M, B.shape[1], K, pa, lda, pb, ldb)
+    if n < 0:
+        raise DgemmError(ERR_INVALID_ARG, "gemm_tf32_workspace_bytes")
+    return int(n)
+
+
+def gemm_tf32_ws(A, B, C, alpha: float = 1.0, beta: float = 0.0, workspace=None, stream=None):
+    """gemm_tf32 for operands whose base or row pitch TMA cannot load: they
+    are copied into ``workspace`` (a CUDA tensor of at least
+    tf32_workspace_bytes(A, B) bytes, 16-byte aligned) first."""
+    pa, lda = _mat(A, "A", torch.float32)
+    pb, ldb = _mat(B, "B", torch.float32)
+    pc, ldc = _mat(C, "C", torch.float32)
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch: A %s, B %s, C %s" % (tuple(A.shape), tuple(B.shape), tuple(C.shape)))
+    pw, nw = 0, 0
+    if workspace is not None:
+        if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
+        pw, nw = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib().gemm_tf32_ws(M, N, K, float(alpha), pa, lda, pb, ldb, float(beta), pc, ldc,
+                            pw or None, nw, _stream(stream))
+    if st != OK:
+        raise DgemmError(st, "gemm_tf32_ws")
+    return C
 
 
 def _gemm16(name, dtype, tn, A, B, C, alpha, beta, stream):

@@ -104,6 +104,49 @@ extern "C" int gemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const flo
 
 namespace {
 
+// Where gemm_tf32_ws puts the repacked operands.  An operand is repacked
+// when TMA cannot describe it (base or row pitch not a multiple of 16 bytes):
+// A becomes M x round_up(K, 4) at offset 0, B K x round_up(N, 32) at a
+// 256-byte boundary after it (columns past N are zeros).  bytes = 0 when neither needs it; -1 if the
+// sizes overflow.
+struct Tf32Repack {
+    bool a = false, b = false;
+    int64_t lda = 0, ldb = 0;
+    int64_t off_b = 0, bytes = 0;
+};
+
+bool tma_ok_f32(const void *p, int64_t ld)
+{
+    return aligned16(p) && (ld * 4) % 16 == 0;
+}
+
+Tf32Repack plan_tf32_repack(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                            const float *B, int64_t ldb)
+{
+    Tf32Repack r;
+    if (M <= 0 || N <= 0 || K <= 0) return r;
+    r.a = !tma_ok_f32(A, lda);
+    r.b = !tma_ok_f32(B, ldb);
+    r.lda = (K + 3) / 4 * 4;
+    // B padded to whole 32-column groups (zeros): the TF32 kernels then load
+    // a stage's B half as one 3-D box
+    r.ldb = (N + 31) / 32 * 32;
+    constexpr int64_t kMax = INT64_MAX / 8;
+    int64_t size_a = 0, size_b = 0;
+    if (r.a) {
+        if (M > kMax / r.lda) return Tf32Repack{false, false, 0, 0, 0, -1};
+        size_a = (M * r.lda * 4 + 255) / 256 * 256;
+    }
+    if (r.b) {
+        if (K > kMax / r.ldb) return Tf32Repack{false, false, 0, 0, 0, -1};
+        size_b = K * r.ldb * 4;
+    }
+    if (size_a > kMax - size_b) return Tf32Repack{false, false, 0, 0, 0, -1};
+    r.off_b = size_a;
+    r.bytes = size_a + size_b;
+    return r;
+}
+
 // The 16-bit entry points: kind selects the input / output type and the
 // layout of B (TN: stored N x K, ldb >= K; NN: stored K x N, ldb >= N).
 int gemm_16bit(int kind, bool bf16, bool nn, int64_t M, int64_t N, int64_t K, float alpha,
@@ -148,6 +191,43 @@ extern "C" int gemm_bf16_nn(int64_t M, int64_t N, int64_t K, float alpha, const 
                             int64_t ldc, cudaStream_t stream)
 {
     return gemm_16bit(kUmmaBF16NN, true, true, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+extern "C" int64_t gemm_tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                             const float *B, int64_t ldb)
+{
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N) return -1;
+    return plan_tf32_repack(M, N, K, A, lda, B, ldb).bytes;
+}
+
+extern "C" int gemm_tf32_ws(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                            const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                            void *workspace, int64_t workspace_bytes, cudaStream_t stream)
+{
+    int st = validate(M, N, K, alpha, A, lda, B, ldb, N, C, ldc);
+    if (st != DGEMM_OK || M == 0 || N == 0) return st;
+    DeviceInfo dev;
+    if ((st = check_device(dev)) != DGEMM_OK) return st;
+    if (K == 0 || alpha == 0.f) return finish(launch_scale_f32(M, N, beta, C, ldc, stream));
+    const Tf32Repack r = plan_tf32_repack(M, N, K, A, lda, B, ldb);
+    if (r.bytes < 0) return DGEMM_ERR_INVALID_ARG;
+    if (r.bytes > 0) {
+        if (!workspace || workspace_bytes < r.bytes || !aligned16(workspace)) return DGEMM_ERR_INVALID_ARG;
+        float *wa = static_cast<float *>(workspace);
+        float *wb = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + r.off_b);
+        if (r.a) {
+            if (!launch_repack_f32(A, M, K, lda, wa, r.lda, stream, dev)) return DGEMM_ERR_LAUNCH;
+            A = wa;
+            lda = r.lda;
+        }
+        if (r.b) {
+            if (!launch_repack_f32(B, K, N, ldb, wb, r.ldb, stream, dev)) return DGEMM_ERR_LAUNCH;
+            B = wb;
+            ldb = r.ldb;
+        }
+    }
+    return finish(launch_umma(kUmmaTF32NN, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev,
+                              r.b ? r.ldb : N));
 }
 
 extern "C" const char *dgemm_status_string(int status)

@@ -41,10 +41,18 @@ const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, cons
 enum UmmaKind { kUmmaF16TN = 0, kUmmaTF32NN = 1, kUmmaBF16TN = 2, kUmmaF16NN = 3, kUmmaBF16NN = 4 };
 
 // Returns nullptr if the launch could not be prepared (e.g. the driver's
-// tensor-map encoder is unavailable).
+// tensor-map encoder is unavailable).  n_b >= N is the number of columns of
+// B the kernels may read (N-major B only; columns N..n_b-1 must be zeros),
+// which lets a padded copy of B take whole 128-byte column groups.
 const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
                         int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc,
-                        cudaStream_t stream, const DeviceInfo &dev);
+                        cudaStream_t stream, const DeviceInfo &dev, int64_t n_b = 0);
+
+// Copy a rows x cols FP32 matrix (row pitch ld_src, any 4-byte alignment)
+// into dst (16-byte aligned, row pitch ld_dst a multiple of 4), writing zeros
+// in columns cols..ld_dst-1; false if the launch failed.
+bool launch_repack_f32(const float *src, int64_t rows, int64_t cols, int64_t ld_src, float *dst,
+                       int64_t ld_dst, cudaStream_t stream, const DeviceInfo &dev);
 
 // Device status word of the tensor-core kernels (see dgemm_device_status).
 int umma_read_status(int clear);

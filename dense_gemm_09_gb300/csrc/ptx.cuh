@@ -348,6 +348,18 @@ __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_b32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
 {
     float v;

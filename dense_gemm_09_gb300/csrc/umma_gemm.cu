@@ -738,6 +738,43 @@ __device__ __forceinline__ void load_old(const Params &p, int64_t row, int64_t c
     }
 }
 
+// C whose base or pitch rules out 16-byte stores: the warp's 32 x 32 chunk
+// (thread t holds row row0 + t) goes through shared memory (row stride 33
+// words: no bank conflicts either way) and is stored row by row with one
+// column per lane, so each store instruction writes one contiguous row
+// segment instead of 32 rows.  Needs 32 x 33 x 4 bytes at `smem`.
+static_assert(32 * 33 * 4 <= 2 * EPI_BOX_BYTES, "a warp's row-by-row staging fits its epilogue boxes");
+
+template <int kKind>
+__device__ __forceinline__ void store_chunk_by_rows(const Params &p, int64_t row0, int64_t col,
+                                                    const uint32_t (&r)[32], uint32_t smem, int lane)
+{
+    using T = Traits<kKind>;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) ptx::st_shared_b32(smem + (static_cast<uint32_t>(lane) * 33u + e) * 4u, r[e]);
+    __syncwarp();
+    const int64_t c = col + lane;
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+        const int64_t row = row0 + i;
+        if (row >= p.M) break;  // warp-uniform
+        const uint32_t u = ptx::ld_shared_b32(smem + (static_cast<uint32_t>(i) * 33u + lane) * 4u);
+        if (c < p.N) {
+            float v = p.alpha * __uint_as_float(u);
+            if constexpr (T::kElem == 2) {
+                uint16_t *dst = reinterpret_cast<uint16_t *>(p.C) + row * p.ldc + c;
+                if (p.beta != 0.f) v = fmaf(p.beta, load1<T::kBF>(dst), v);
+                *dst = round1<T::kBF>(v);
+            } else {
+                float *dst = reinterpret_cast<float *>(p.C) + row * p.ldc + c;
+                if (p.beta != 0.f) v = fmaf(p.beta, *dst, v);
+                *dst = v;
+            }
+        }
+    }
+    __syncwarp();  // the buffer is reused by the next chunk
+}
+
 // Drain one warp's 32 accumulator rows (TMEM address taddr, first row row0)
 // x BN columns from n0 into C.  nbox counts the boxes this warp has stored.
 template <int kKind>
@@ -753,7 +790,10 @@ __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *t
             __syncwarp();  // tcgen05.ld is warp-collective (.sync.aligned)
             ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
             ptx::tmem_ld_wait();
-            store_chunk<kKind>(p, row, n0 + c * 32, r);
+            if (p.vec_c)
+                store_chunk<kKind>(p, row, n0 + c * 32, r);
+            else
+                store_chunk_by_rows<kKind>(p, row0, n0 + c * 32, r, box_smem, lane);
         }
         return;
     }
@@ -1761,10 +1801,18 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
 }
 
 template <int kKind>
+constexpr bool T_is_n_major()
+{
+    return Traits<kKind>::kBNMajor;
+}
+
+template <int kKind>
 const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
                         const void *B, int64_t ldb, float beta, void *C, int64_t ldc,
-                        cudaStream_t stream, const DeviceInfo &dev)
+                        cudaStream_t stream, const DeviceInfo &dev, int64_t n_b)
 {
+    // columns of an N-major B the loads may cover (zeros past N)
+    const int64_t NB = T_is_n_major<kKind>() && n_b > N ? n_b : N;
     using T = Traits<kKind>;
     constexpr int es = T::kElem;
     const CUtensorMapDataType dt = T::kTf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -1792,10 +1840,10 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
             if constexpr (T::kBNMajor) {
                 const CUtensorMapSwizzle sw =
                     T::kTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
-                if (N % T::kNBox == 0 &&
+                if (NB % T::kNBox == 0 &&
                     make_map_3d(m, dt, B,
                                 {static_cast<uint64_t>(T::kNBox), static_cast<uint64_t>(K),
-                                 static_cast<uint64_t>(N / T::kNBox)},
+                                 static_cast<uint64_t>(NB / T::kNBox)},
                                 {static_cast<uint64_t>(ldb * es), static_cast<uint64_t>(T::kNBox * es)},
                                 {static_cast<uint32_t>(T::kNBox), static_cast<uint32_t>(T::BK),
                                  static_cast<uint32_t>(bn / T::kNBox)},
@@ -1803,7 +1851,7 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
                     *b3d = 1;
                     return true;
                 }
-                return make_map(m, dt, B, N, K, ldb * es, T::kNBox, T::BK, sw);
+                return make_map(m, dt, B, NB, K, ldb * es, T::kNBox, T::BK, sw);
             } else {
                 return make_map(m, dt, B, K, N, ldb * es, T::BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
             }
@@ -1828,19 +1876,19 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
 
 const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
                         int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc,
-                        cudaStream_t stream, const DeviceInfo &dev)
+                        cudaStream_t stream, const DeviceInfo &dev, int64_t n_b)
 {
     switch (kind) {
     case kUmmaF16TN:
-        return launch_kind<kF16>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+        return launch_kind<kF16>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev, n_b);
     case kUmmaTF32NN:
-        return launch_kind<kTF32>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+        return launch_kind<kTF32>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev, n_b);
     case kUmmaBF16TN:
-        return launch_kind<kBF16>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+        return launch_kind<kBF16>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev, n_b);
     case kUmmaF16NN:
-        return launch_kind<kF16NN>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+        return launch_kind<kF16NN>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev, n_b);
     case kUmmaBF16NN:
-        return launch_kind<kBF16NN>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev);
+        return launch_kind<kBF16NN>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev, n_b);
     default:
         return nullptr;
     }

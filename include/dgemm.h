@@ -99,6 +99,46 @@ int gemm_tf32(int64_t M, int64_t N, int64_t K, float alpha,
               float beta, float *C, int64_t ldc, cudaStream_t stream);
 
 /*
+ * gemm_tf32_ws -- gemm_tf32 with a caller-provided scratch buffer for
+ * operands that the tensor-memory-access (TMA) loads cannot describe: a base
+ * that is not 16-byte aligned, or a leading dimension whose byte size is not
+ * a multiple of 16 (e.g. lda = K = 4095).  Such an operand is first copied,
+ * bit for bit, into the workspace with a padded pitch (A as M x
+ * round_up(K, 4), B as K x round_up(N, 32) with zeros past column N), then
+ * the TMA kernels run on the copy.  This replaces gemm_tf32's slower
+ * element-wise loading path for those operands; results are the same as
+ * gemm_tf32 on an aligned copy of the operands.
+ *   workspace       : device buffer, 16-byte aligned, owned by the caller; it
+ *                     must not overlap A, B or C and must stay untouched
+ *                     until the stream has passed the call.  May be NULL
+ *                     when gemm_tf32_workspace_bytes returns 0.
+ *   workspace_bytes : its size in bytes.
+ * Returns DGEMM_ERR_INVALID_ARG (nothing launched) when the workspace is
+ * needed but is NULL, smaller than gemm_tf32_workspace_bytes() or not
+ * 16-byte aligned; otherwise as gemm_tf32.  The call itself allocates
+ * nothing.
+ * Source: the operation of gemm_tf32; the repack is this library's way of
+ * feeding the TMA loads ("SGEMM CUDA代码学习", "第 5 步", stages operands
+ * through shared memory with asynchronous copies that need aligned
+ * addresses as well).
+ */
+int gemm_tf32_ws(int64_t M, int64_t N, int64_t K, float alpha,
+                 const float *A, int64_t lda, const float *B, int64_t ldb,
+                 float beta, float *C, int64_t ldc,
+                 void *workspace, int64_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * gemm_tf32_workspace_bytes -- workspace gemm_tf32_ws needs for these
+ * operands: 0 when both A and B can be loaded as they are, else the bytes
+ * of their padded copies; -1 for negative sizes, a leading dimension below
+ * its row length, or sizes whose copies would not fit in 2^63 bytes.  Host
+ * arithmetic only (no device access); the pointers are only looked at for
+ * their alignment.
+ */
+int64_t gemm_tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                  const float *B, int64_t ldb);
+
+/*
  * gemm_f16_tn -- HGEMM in the TN layout: C = alpha * A * B^T + beta * C.
  *   A, lda  : device, IEEE binary16, M x K row-major, (m, k) at A[m*lda + k].
  *   B, ldb  : device, IEEE binary16, stored N x K row-major, so the logical

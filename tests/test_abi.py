@@ -121,3 +121,39 @@ def test_tune_next_validates_on_host(L):
     assert L.dgemm_tune_next(3, 128, 9) == 1     # split above 8
     assert L.dgemm_tune_next(3, 128, 4) == 0
     assert L.dgemm_tune_next(0, 0, 0) == 0       # back to automatic
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 8, 8, 1.0, P, 8, P, 8, 0.0, P, 8),      # negative M
+    (8, 8, 8, 1.0, P, 7, P, 8, 0.0, P, 8),       # lda < K
+    (8, 8, 8, 1.0, P, 8, P, 7, 0.0, P, 8),       # ldb < N
+    (8, 8, 8, 1.0, P, 8, P, 8, 0.0, 0, 8),       # C null
+])
+def test_tf32_ws_invalid_arguments_rejected_on_host(L, args):
+    assert L.gemm_tf32_ws(*args, P, 1 << 20, None) == 1
+
+
+def test_tf32_ws_empty_problem_returns_ok_without_device(L):
+    assert L.gemm_tf32_ws(0, 8, 8, 1.0, 0, 8, 0, 8, 0.0, 0, 8, None, 0, None) == 0
+
+
+def test_tf32_workspace_bytes_host_arithmetic(L):
+    f = L.gemm_tf32_workspace_bytes
+    # TMA-describable operands need no copy
+    assert f(8192, 8192, 4096, P, 4096, P, 8192) == 0
+    # the ragged workload (lda = 4095, ldb = 8193 floats): A as 8191 x 4096,
+    # then B as 4095 x 8224 (whole 32-column groups) from the next 256-byte
+    # boundary
+    a = 8191 * 4096 * 4
+    assert f(8191, 8193, 4095, P, 4095, P, 8193) == (a + 255) // 256 * 256 + 4095 * 8224 * 4
+    # only A (base off a 16-byte boundary): 5 x 8 floats, padded to 256 bytes
+    assert f(5, 8, 8, P + 4, 8, P, 8) == 256
+    # only B (pitch of 9 floats): 8 x 32 floats
+    assert f(5, 9, 8, P, 8, P, 9) == 8 * 32 * 4
+    # K or M == 0: nothing to copy
+    assert f(0, 9, 8, P + 4, 8, P, 9) == 0
+    assert f(5, 9, 0, P + 4, 8, P, 9) == 0
+    # invalid sizes, and copies past 2^63 bytes
+    assert f(-1, 1, 1, P, 1, P, 1) == -1
+    assert f(4, 4, 4, P, 3, P, 4) == -1
+    assert f(2**40, 4, 2**30, P, 2**30 + 1, P, 4) == -1
