@@ -76,6 +76,8 @@ def lib():
         L.gemm_tf32_ws.restype = ci
         L.gemm_tf32_workspace_bytes.argtypes = [i64, i64, i64, vp, i64, vp, i64]
         L.gemm_tf32_workspace_bytes.restype = i64
+        L.gemm_tf32_noalloc.argtypes = sig
+        L.gemm_tf32_noalloc.restype = ci
         _lib = L
         return L
 
@@ -196,6 +198,24 @@ def gemm_tf32_ws(A, B, C, alpha: float = 1.0, beta: float = 0.0, workspace=None,
     if st != OK:
         raise DgemmError(st, "gemm_tf32_ws")
     return C
+
+
+# Bytes of the library's fixed scratch behind gemm_tf32_noalloc (see
+# DGEMM_NOALLOC_SCRATCH_BYTES in include/dgemm.h).
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def gemm_tf32_noalloc(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """gemm_tf32_ws for callers that cannot allocate device memory: the
+    copies of operands TMA cannot load go to a fixed 64 MiB scratch array
+    inside the library instead of a caller workspace.  Calls that overlap on
+    the GPU share that array and race; operands whose copies need more than
+    NOALLOC_SCRATCH_BYTES are refused."""
+    need = tf32_workspace_bytes(A, B)
+    if need > NOALLOC_SCRATCH_BYTES:
+        raise DgemmError(ERR_INVALID_ARG, "gemm_tf32_noalloc (the operands' padded copies need %d bytes; "
+                         "the fixed scratch holds %d)" % (need, NOALLOC_SCRATCH_BYTES))
+    return _nn("gemm_tf32_noalloc", A, B, C, alpha, beta, stream)
 
 
 def _gemm16(name, dtype, tn, A, B, C, alpha, beta, stream):

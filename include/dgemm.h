@@ -138,6 +138,39 @@ int gemm_tf32_ws(int64_t M, int64_t N, int64_t K, float alpha,
 int64_t gemm_tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                                   const float *B, int64_t ldb);
 
+/* Size of the fixed scratch array behind gemm_tf32_noalloc (64 MiB). */
+#define DGEMM_NOALLOC_SCRATCH_BYTES (64LL * 1024 * 1024)
+
+/*
+ * gemm_tf32_noalloc -- gemm_tf32_ws without a workspace argument, for callers
+ * that cannot allocate device memory and so cannot provide one: for example
+ * code running inside a host framework whose memory pool owns all of the
+ * device's memory and refuses side allocations, or a latency-critical loop
+ * in which an allocation (which may synchronise the device) is not
+ * acceptable.  The caller still passes A, B and C as for gemm_tf32.
+ * There is no counterpart in the pages: this is a property of the library,
+ * not of the method.
+ *   Scratch: a fixed array of DGEMM_NOALLOC_SCRATCH_BYTES in the library's
+ *     device memory, which every GPU that loads the library holds until the
+ *     process exits.  The call allocates nothing and frees nothing.
+ *   Limit: operands whose padded copies need more than
+ *     DGEMM_NOALLOC_SCRATCH_BYTES (see gemm_tf32_workspace_bytes) are
+ *     rejected with DGEMM_ERR_INVALID_ARG and nothing is launched.  Operands
+ *     that need no copy run as gemm_tf32_ws does, without touching it.
+ *   Set-up: the first call on each device, made with that device current,
+ *     looks up the array's device address; make that first call before any
+ *     stream capture.  DGEMM_ERR_LAUNCH if the lookup fails.
+ *   Sharing: every call uses the same array and each rewrites all of it that
+ *     it reads, so no state carries over from one call to the next; two calls
+ *     whose work overlaps on the GPU (different streams, or unordered calls
+ *     from different host threads) race on the array and may corrupt each
+ *     other's results.
+ * Otherwise as gemm_tf32_ws.
+ */
+int gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                      const float *A, int64_t lda, const float *B, int64_t ldb,
+                      float beta, float *C, int64_t ldc, cudaStream_t stream);
+
 /*
  * gemm_f16_tn -- HGEMM in the TN layout: C = alpha * A * B^T + beta * C.
  *   A, lda  : device, IEEE binary16, M x K row-major, (m, k) at A[m*lda + k].
