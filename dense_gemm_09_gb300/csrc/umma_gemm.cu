@@ -64,10 +64,15 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int STAGES = 4;
+// The TMA-fed single-CTA kernel sizes its ring at run time: stages of
+// A_TILE_BYTES + bn * ROW_BYTES, as many as fit (at most MAX_STAGES) --
+// narrow tiles keep more bytes in flight.  The non-TMA producers use STAGES
+// stages of STAGE_BYTES.
 constexpr int ROW_BYTES = 128;                     // one swizzled row
 constexpr int A_TILE_BYTES = BM * ROW_BYTES;       // 16 KB
 constexpr int B_TILE_BYTES = BN * ROW_BYTES;       // 32 KB
 constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int MAX_STAGES = 8;
 constexpr int TMEM_COLS = 2 * BN;                  // two f32 accumulators
 constexpr int kGroupN = 8;                         // tile-order group width
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s, default wait bound
@@ -157,8 +162,8 @@ struct WaitCtl {
 };
 
 struct Ctrl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
@@ -195,6 +200,9 @@ struct Params {
     // for 16-bit N-major B) from 32 to 256; the CTA-pair and register-path
     // kernels use 256.  The MMA is 128 x bn x UMMA_K.
     int bn;
+    // single-CTA kernel: stages in its ring and bytes per stage (1024-byte
+    // multiples); the TMA producer uses A_TILE_BYTES + bn * ROW_BYTES
+    int stages, stage_bytes;
     // CTA-pair kernel with N-major B: the stage's B half comes as one 3-D box
     // (column group of 128 bytes x BK rows x 128 / kNBox groups) instead of
     // 128 / kNBox 2-D boxes
@@ -324,7 +332,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
             }
             const uint32_t full = ptx::smem_addr(&ctrl->full[stage]);
             ptx::mbar_arrive_expect_tx(full, A_TILE_BYTES + p.bn * ROW_BYTES);
-            const uint32_t sa = smem_base + stage * STAGE_BYTES;
+            const uint32_t sa = smem_base + stage * static_cast<uint32_t>(p.stage_bytes);
             const uint32_t sb = sa + A_TILE_BYTES;
             const int32_t kc = static_cast<int32_t>(kb * T::BK);
             ptx::tma_load_2d(sa, tmap_a, full, kc, static_cast<int32_t>(m0));
@@ -343,7 +351,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
             }
             issued |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) {
+            if (++stage == static_cast<uint32_t>(p.stages)) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -351,7 +359,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
     }
     if (!ok) {
         // Do not leave while TMA may still be writing into this CTA's smem.
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < p.stages; ++s)
             if ((issued >> s) & 1u)
                 drain_wait(ptx::smem_addr(&ctrl->full[s]), (issued_phase >> s) & 1u);
     }
@@ -560,7 +568,7 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t sa = smem_base + stage * STAGE_BYTES;
+            const uint32_t sa = smem_base + stage * static_cast<uint32_t>(p.stage_bytes);
             const uint32_t sb = sa + A_TILE_BYTES;
 #pragma unroll
             for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
@@ -580,7 +588,7 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
                                  (kb != sc.kb0 || k != 0) ? 1u : 0u);
             }
             ptx::umma_commit(ptx::smem_addr(&ctrl->empty[stage]));
-            if (++stage == STAGES) {
+            if (++stage == static_cast<uint32_t>(p.stages)) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -1018,7 +1026,7 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < MAX_STAGES; ++s) {
             ptx::mbar_init(ptx::smem_addr(&ctrl->full[s]), kTma ? 1 : 32 * producer_warps<kTma>());
             ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), 1);
         }
@@ -1549,6 +1557,8 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, 
     p.bn = BN;
     p.tma_store = 0;
     p.b3d = 0;
+    p.stages = STAGES;
+    p.stage_bytes = STAGE_BYTES;
     p.inject_stall = t_inject_limit_ns ? 1 : 0;
     p.splitk = 1;
     p.wait_limit_ns = t_inject_limit_ns ? t_inject_limit_ns : kWaitLimitNs;
@@ -1750,6 +1760,17 @@ const char *variant_name(int variant, int bn = BN, int split = 1)
     return names[2 + w * 9 + S].c_str();
 }
 
+// The single-CTA TMA kernel's ring for tile width p.bn: as many stages of
+// A_TILE_BYTES + bn * ROW_BYTES as fit in the ring space (at most
+// MAX_STAGES).  Split-K launches do not use the epilogue boxes (their
+// partials meet in the ring), so their ring may extend over them.
+void set_ring(Params &p, bool split)
+{
+    p.stage_bytes = A_TILE_BYTES + p.bn * ROW_BYTES;
+    const int space = STAGES * STAGE_BYTES + (split ? EPI_BYTES : 0);
+    p.stages = std::min(MAX_STAGES, space / p.stage_bytes);
+}
+
 // TMA-capable operands.  ma: A with 128-row boxes; mb_pair: B boxes of the
 // pair kernel (null if B cannot be described); make_b(bn, map) builds B's map
 // for 128 x bn tiles.
@@ -1792,10 +1813,12 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
     p.b3d = b3d;
     if (cfg.variant == kVariantSplit) {
         p.splitk = cfg.split;
+        set_ring(p, true);
         if (launch_splitk<kKind>(ma, mb, mc, p, stream))
             return variant_name<kKind>(kVariantSplit, cfg.bn, cfg.split);
         p.splitk = 1;
     }
+    set_ring(p, false);
     return launch<kKind, true>(ma, mb, mc, p, stream, dev) ? variant_name<kKind>(kVariantSingle, cfg.bn)
                                                            : nullptr;
 }
