@@ -163,6 +163,19 @@ def _traffic_for(kernel_file: str, kernel_key: str, shape):
     return e.get("bytes_per_launch") if e.get("source_sha256") == sha else None
 
 
+def _config(paths_run, shape, world, l2=None):
+    """The workload description both arms print."""
+    Mx, Nx, Kx = shape
+    default_run = tuple(paths_run) == PATHS and (Mx, Nx, Kx) == (M, N, K)
+    return {"workload": ("gemm_f32_tf32_f16tn_8192x8192x4096" if default_run else
+                         "gemm_%s_%dx%dx%d" % ("+".join(paths_run), Mx, Nx, Kx)),
+            "M": Mx, "N": Nx, "K": Kx,
+            "alpha": 1.0, "beta": 0.0, "layout": "row-major NN (f32, tf32); TN (f16)",
+            "step": " + ".join("one " + p for p in paths_run),
+            "l2": l2 or "flushed before every GEMM (512 MiB write + 256 MiB read, outside the timed events)",
+            "parallelism": "replicas x%d" % world}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -343,13 +356,7 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32+tf32+f16(f32 acc)" if default_run
         else "+".join(paths_run),
         "data": "synthetic (seeded uniform[-1,1) f32; N(0,1)/sqrt(K) f16)",
-        "config": {"workload": ("gemm_f32_tf32_f16tn_8192x8192x4096" if default_run else
-                                "gemm_%s_%dx%dx%d" % ("+".join(paths_run), Mx, Nx, Kx)),
-                   "M": Mx, "N": Nx, "K": Kx,
-                   "alpha": 1.0, "beta": 0.0, "layout": "row-major NN (f32, tf32); TN (f16)",
-                   "step": " + ".join("one " + p for p in paths_run),
-                   "l2": "flushed before every GEMM (512 MiB write + 256 MiB read, outside the timed events)",
-                   "parallelism": "replicas x%d" % world},
+        "config": _config(paths_run, (Mx, Nx, Kx), world),
         "paths": paths,
         "roofline": roofline,
         "clocks": clocks,
@@ -440,8 +447,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 accumulation over f32 / tf32 / f16 operand values",
         "data": "synthetic (seeded uniform[-1,1) f32; N(0,1)/sqrt(K) f16)",
-        "config": {"workload": "gemm_f32_tf32_f16tn_8192x8192x4096", "M": M, "N": N, "K": K,
-                   "alpha": 1.0, "beta": 0.0},
+        "config": _config(PATHS, (M, N, K), world,
+                          l2="not applicable: the oracle runs on the host cores"),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
                          "kind": "oracle",
                          "sample": "%d full rows of C over %d steps (%.1f s per step budget)"
