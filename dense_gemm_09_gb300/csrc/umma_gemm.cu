@@ -747,11 +747,12 @@ __device__ __forceinline__ void load_old(const Params &p, int64_t row, int64_t c
 }
 
 // C whose base or pitch rules out 16-byte stores: the warp's 32 x 32 chunk
-// (thread t holds row row0 + t) goes through shared memory (row stride 33
-// words: no bank conflicts either way) and is stored row by row with one
-// column per lane, so each store instruction writes one contiguous row
-// segment instead of 32 rows.  Needs 32 x 33 x 4 bytes at `smem`.
-static_assert(32 * 33 * 4 <= 2 * EPI_BOX_BYTES, "a warp's row-by-row staging fits its epilogue boxes");
+// (thread t holds row row0 + t) goes through shared memory and is stored row
+// by row with one column per lane, so each store instruction writes one
+// contiguous row segment instead of 32 rows.  Word e of row t sits at
+// column e ^ t, so both the row-wise writes and the column-wise reads hit 32
+// different banks.  Needs 32 x 32 x 4 bytes (one epilogue box) at `smem`.
+static_assert(32 * 32 * 4 <= EPI_BOX_BYTES, "a warp's row-by-row staging fits one epilogue box");
 
 template <int kKind>
 __device__ __forceinline__ void store_chunk_by_rows(const Params &p, int64_t row0, int64_t col,
@@ -759,14 +760,15 @@ __device__ __forceinline__ void store_chunk_by_rows(const Params &p, int64_t row
 {
     using T = Traits<kKind>;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) ptx::st_shared_b32(smem + (static_cast<uint32_t>(lane) * 33u + e) * 4u, r[e]);
+    for (int e = 0; e < 32; ++e)
+        ptx::st_shared_b32(smem + (static_cast<uint32_t>(lane) * 32u + (static_cast<uint32_t>(e) ^ lane)) * 4u, r[e]);
     __syncwarp();
     const int64_t c = col + lane;
 #pragma unroll 4
     for (int i = 0; i < 32; ++i) {
         const int64_t row = row0 + i;
         if (row >= p.M) break;  // warp-uniform
-        const uint32_t u = ptx::ld_shared_b32(smem + (static_cast<uint32_t>(i) * 33u + lane) * 4u);
+        const uint32_t u = ptx::ld_shared_b32(smem + (static_cast<uint32_t>(i) * 32u + (lane ^ static_cast<uint32_t>(i))) * 4u);
         if (c < p.N) {
             float v = p.alpha * __uint_as_float(u);
             if constexpr (T::kElem == 2) {
@@ -784,16 +786,20 @@ __device__ __forceinline__ void store_chunk_by_rows(const Params &p, int64_t row
 }
 
 // Drain one warp's 32 accumulator rows (TMEM address taddr, first row row0)
-// x BN columns from n0 into C.  nbox counts the boxes this warp has stored.
-template <int kKind>
+// x BN columns from n0 into C.  nbox counts the boxes this warp has stored;
+// kBoxes staging boxes of EPI_BOX_BYTES at box_smem take turns (2: a box is
+// filled while the previous one's store is still reading).  cols: columns to
+// drain (p.bn by default).
+template <int kKind, int kBoxes = 2>
 __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *tmap_c,
                                            uint32_t taddr, int64_t row0, int64_t n0,
-                                           uint32_t box_smem, int lane, uint32_t &nbox)
+                                           uint32_t box_smem, int lane, uint32_t &nbox, int cols = 0)
 {
+    if (cols == 0) cols = p.bn;
     const int64_t row = row0 + lane;
     if (!p.tma_store) {
 #pragma unroll 1
-        for (int c = 0; c < p.bn / 32; ++c) {
+        for (int c = 0; c < cols / 32; ++c) {
             uint32_t r[32];
             __syncwarp();  // tcgen05.ld is warp-collective (.sync.aligned)
             ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
@@ -807,7 +813,7 @@ __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *t
     }
     constexpr int COLS = box_cols<kKind>();
 #pragma unroll 1
-    for (int b = 0; b < p.bn / COLS; ++b) {
+    for (int b = 0; b < cols / COLS; ++b) {
         const int64_t col0 = n0 + b * COLS;
         uint32_t r[COLS];
         __syncwarp();
@@ -825,8 +831,8 @@ __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *t
 #pragma unroll
             for (int e = 0; e < COLS; ++e) v[e] = fmaf(p.beta, old[e], v[e]);
         }
-        const uint32_t buf = box_smem + (nbox & 1u) * EPI_BOX_BYTES;
-        if (lane == 0 && nbox >= 2) ptx::bulk_wait_read<1>();  // this buffer's last store read it
+        const uint32_t buf = box_smem + (nbox % kBoxes) * EPI_BOX_BYTES;
+        if (lane == 0 && nbox >= kBoxes) ptx::bulk_wait_read<kBoxes - 1>();  // this box's last store read it
         __syncwarp();
         const uint32_t rowbase = buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
@@ -1128,6 +1134,14 @@ constexpr int PAIR_BM = 2 * BM;                    // rows per pair tile
 constexpr int PAIR_HALF_BYTES = 128 * ROW_BYTES;   // 16 KB: 128 rows of A or of B
 constexpr int PAIR_STAGE_BYTES = 2 * PAIR_HALF_BYTES;
 constexpr int PAIR_THREADS = 224;
+// Wide tiles (kWide = 2) drain a 512-column accumulator that the next tile's
+// MMAs wait for, so they add four epilogue warps (7-10): each of the eight
+// drains one lane quarter x 256 columns, with one staging box each.
+template <int kWide>
+constexpr int pair_threads()
+{
+    return kWide == 2 ? PAIR_THREADS + 4 * 32 : PAIR_THREADS;
+}
 constexpr int PAIR_MMA_WARP = 1;
 constexpr int PAIR_WAITER_WARP = 6;
 constexpr uint32_t PAIR_HANDOFF_THREADS = 64;  // warps 1 and 6 on named barriers 1..PAIR_STAGES
@@ -1168,12 +1182,26 @@ __device__ __forceinline__ void pair_tile(int64_t t, const Params &p, uint32_t r
     n0 = n0 * kPairs + static_cast<int64_t>(rank >> 1) * BN;
 }
 
-template <int kKind, int kPairs>
+// Pair tiles of 256 x (256 * kWide): with kWide = 2 each MMA step is two
+// MMAs of N = 256 into one 512-column accumulator (the whole TMEM), so each
+// CTA loads 16 KB of A and 32 KB of B per stage for twice the MMA work --
+// a quarter fewer bytes per flop into every SM -- at the price of a single
+// accumulator, whose drain the next tile's MMAs wait for.
+template <int kWide>
+struct PairShape {
+    static constexpr int kStageBytes = PAIR_HALF_BYTES * (1 + kWide);  // A half + kWide B halves
+    static constexpr int kStages = PAIR_STAGES * PAIR_STAGE_BYTES / kStageBytes;  // 6 or 4
+    static constexpr int kAccs = 2 / kWide;                                 // TMEM accumulators
+    static constexpr int kAccCols = BN * kWide;
+};
+
+template <int kKind, int kPairs, int kWide>
 __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
                                               const Params &p, uint32_t smem_base, PairCtrl *ctrl,
                                               uint32_t rank, WaitCtl *wc)
 {
     using T = Traits<kKind>;
+    using S = PairShape<kWide>;
     constexpr int kCtas = 2 * kPairs;
     constexpr int kRowsA = 128 / kPairs;  // A rows this CTA loads per stage
     constexpr uint16_t kHalfMask = kPairs == 1 ? 0x1 : 0x5;  // the even CTA of every pair
@@ -1193,9 +1221,8 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
             }
             const uint32_t full_local = ptx::smem_addr(&ctrl->full[stage]);
             const uint32_t full = ptx::mapa(full_local, leader);  // the pair leader's barrier
-            if (half == 0) ptx::mbar_arrive_expect_tx(full_local, 2 * PAIR_STAGE_BYTES);
-            const uint32_t sa = smem_base + stage * PAIR_STAGE_BYTES;
-            const uint32_t sb = sa + PAIR_HALF_BYTES;
+            if (half == 0) ptx::mbar_arrive_expect_tx(full_local, 2 * S::kStageBytes);
+            const uint32_t sa = smem_base + stage * S::kStageBytes;
             const int32_t kc = static_cast<int32_t>(kb * T::BK);
             const int32_t ma = static_cast<int32_t>(m0 + half * 128 + pair * kRowsA);
             if constexpr (kPairs == 1)
@@ -1203,22 +1230,26 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
             else
                 ptx::tma_load_2d_pair_multicast(sa + pair * kRowsA * ROW_BYTES, tmap_a, full, kc, ma,
                                                 static_cast<uint16_t>(kHalfMask << half));
-            const int64_t nb = n0 + half * 128;  // this CTA's half of B
-            if constexpr (!T::kBNMajor) {
-                ptx::tma_load_2d_pair(sb, tmap_b, full, kc, static_cast<int32_t>(nb));
-            } else if (p.b3d) {
-                // one instruction instead of four (TF32) or two (16-bit NN):
-                // the producer thread's issue rate bounds the TF32 stage rate
-                ptx::tma_load_3d_pair(sb, tmap_b, full, 0, kc, static_cast<int32_t>(nb / T::kNBox));
-            } else {
 #pragma unroll
-                for (int c = 0; c < 128 / T::kNBox; ++c)
-                    ptx::tma_load_2d_pair(sb + c * T::kNBoxBytes, tmap_b, full,
-                                          static_cast<int32_t>(nb + c * T::kNBox), kc);
+            for (int w = 0; w < kWide; ++w) {
+                const uint32_t sb = sa + (1 + w) * PAIR_HALF_BYTES;
+                const int64_t nb = n0 + w * BN + half * 128;  // this CTA's half of B, MMA w
+                if constexpr (!T::kBNMajor) {
+                    ptx::tma_load_2d_pair(sb, tmap_b, full, kc, static_cast<int32_t>(nb));
+                } else if (p.b3d) {
+                    // one instruction instead of four (TF32) or two (16-bit NN):
+                    // the producer thread's issue rate bounds the TF32 stage rate
+                    ptx::tma_load_3d_pair(sb, tmap_b, full, 0, kc, static_cast<int32_t>(nb / T::kNBox));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 128 / T::kNBox; ++c)
+                        ptx::tma_load_2d_pair(sb + c * T::kNBoxBytes, tmap_b, full,
+                                              static_cast<int32_t>(nb + c * T::kNBox), kc);
+                }
             }
             issued |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-            if (++stage == PAIR_STAGES) {
+            if (++stage == S::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -1227,7 +1258,7 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
     if (!ok && half == 0) {
         // The leader's barrier counts both CTAs' bytes: wait (bounded) for
         // the loads in flight before the pair leaves.
-        for (int s = 0; s < PAIR_STAGES; ++s)
+        for (int s = 0; s < S::kStages; ++s)
             if ((issued >> s) & 1u)
                 drain_wait(ptx::smem_addr(&ctrl->full[s]), (issued_phase >> s) & 1u);
     }
@@ -1238,9 +1269,10 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
 // named barrier 1 + stage.  The barrier's OR-reduction carries the abort flag
 // both ways, so each side runs through the same number of hand-offs and
 // neither can be left waiting on the other after a time-out.
-template <int kKind, int kPairs>
+template <int kKind, int kPairs, int kWide>
 __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int lane, WaitCtl *wc)
 {
+    using S = PairShape<kWide>;
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
     uint32_t stage = 0, phase = 0;
@@ -1253,7 +1285,7 @@ __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int
                 abort = __shfl_sync(0xffffffffu, ok ? 0 : 1, 0) != 0;
             }
             abort = ptx::bar_red_or(1 + stage, PAIR_HANDOFF_THREADS, abort);
-            if (++stage == PAIR_STAGES) {
+            if (++stage == S::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -1266,11 +1298,12 @@ __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int
 // stage's release to the "empty" barriers of every CTA of the cluster (with
 // two pairs, both pairs' producers write each CTA's ring); per tile it waits
 // for a free accumulator and commits "tmem_full" to its own pair.
-template <int kKind, int kPairs>
+template <int kKind, int kPairs, int kWide>
 __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, PairCtrl *ctrl,
                                          uint32_t tmem_base, uint32_t rank, int lane, WaitCtl *wc)
 {
     using T = Traits<kKind>;
+    using S = PairShape<kWide>;
     constexpr uint16_t kAll = static_cast<uint16_t>((1u << (2 * kPairs)) - 1u);
     const uint16_t kPair = static_cast<uint16_t>(0x3u << rank);
     const int64_t num_tiles = p.tiles_m * p.tiles_n;
@@ -1287,34 +1320,40 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
                 ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u, wc);
             abort = __shfl_sync(0xffffffffu, ok ? 0 : 1, 0) != 0;
         }
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * S::kAccCols;
         for (int64_t kb = 0; kb < p.num_kb; ++kb) {
             abort = ptx::bar_red_or(1 + stage, PAIR_HANDOFF_THREADS, abort);
             if (!abort) {
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t sa = smem_base + stage * PAIR_STAGE_BYTES;
-                    const uint32_t sb = sa + PAIR_HALF_BYTES;
+                    const uint32_t sa = smem_base + stage * S::kStageBytes;
 #pragma unroll
                     for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
                         const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
-                        uint64_t db;
-                        if constexpr (!T::kBNMajor)
-                            db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
-                        else
-                            db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
-                        ptx::umma_pair<kKind>(d_tmem, da, db, pair_idesc<kKind>(), (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int w = 0; w < kWide; ++w) {
+                            const uint32_t sb = sa + (1 + w) * PAIR_HALF_BYTES;
+                            uint64_t db;
+                            if constexpr (!T::kBNMajor)
+                                db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
+                            else
+                                db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
+                            ptx::umma_pair<kKind>(d_tmem + w * BN, da, db, pair_idesc<kKind>(),
+                                                  (kb | k) != 0 ? 1u : 0u);
+                        }
                     }
                     ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), kAll);
                 }
                 __syncwarp();
             }
-            if (++stage == PAIR_STAGES) stage = 0;
+            if (++stage == S::kStages) stage = 0;
         }
         if (!abort && lane == 0) ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->tmem_full[acc]), kPair);
         __syncwarp();
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == S::kAccs) {
+            acc = 0;
+            acc_phase ^= 1u;
+        }
     }
     if (lane == 0) {
         ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->mma_done), static_cast<uint16_t>(1u << rank));
@@ -1323,7 +1362,7 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
     __syncwarp();
 }
 
-template <int kKind, int kPairs>
+template <int kKind, int kPairs, int kWide>
 __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap *tmap_c,
                                               PairCtrl *ctrl, uint32_t tmem_base, uint32_t epi_smem,
                                               uint32_t rank, int warp, int lane, WaitCtl *wc)
@@ -1332,6 +1371,10 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap
     const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
     const uint32_t quarter = static_cast<uint32_t>(warp & 3);
     const uint32_t leader = rank & ~1u;
+    // kWide = 2: warps 2-5 drain columns 0-255, warps 7-10 columns 256-511
+    const uint32_t colhalf = kWide == 2 && warp >= 7 ? 1u : 0u;
+    const uint32_t box = kWide == 2 ? epi_smem + static_cast<uint32_t>(warp - (warp >= 7 ? 3 : 2)) * EPI_BOX_BYTES
+                                    : epi_smem + quarter * 2 * EPI_BOX_BYTES;
     uint32_t acc = 0, acc_phase = 0, nbox = 0;
     for (int64_t t = cluster; t < num_tiles; t += clusters) {
         int64_t m0, n0;
@@ -1340,21 +1383,26 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * BN;
-        drain_rows<kKind>(p, tmap_c, taddr, m0 + (rank & 1u) * 128 + quarter * 32, n0,
-                          epi_smem + quarter * 2 * EPI_BOX_BYTES, lane, nbox);
+        const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * PairShape<kWide>::kAccCols;
+        if constexpr (kWide == 2)
+            drain_rows<kKind, 1>(p, tmap_c, taddr + colhalf * BN, m0 + (rank & 1u) * 128 + quarter * 32,
+                                 n0 + colhalf * BN, box, lane, nbox, BN);
+        else
+            drain_rows<kKind>(p, tmap_c, taddr, m0 + (rank & 1u) * 128 + quarter * 32, n0, box, lane, nbox);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0)
             ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_addr(&ctrl->tmem_empty[acc]), leader));
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == PairShape<kWide>::kAccs) {
+            acc = 0;
+            acc_phase ^= 1u;
+        }
     }
     if (lane == 0) ptx::bulk_wait<0>();  // stores done before the CTA leaves
 }
 
-template <int kKind, int kPairs>
-__global__ void __launch_bounds__(PAIR_THREADS, 1)
+template <int kKind, int kPairs, int kWide>
+__global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     umma_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, const Params p)
@@ -1374,7 +1422,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_full[a]), 1);
-            ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_empty[a]), 8);
+            ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_empty[a]), 8 * kWide);  // epilogue warps x 2 CTAs
         }
         ptx::mbar_init(ptx::smem_addr(&ctrl->mma_done), 1);
         ptx::mbar_init(ptx::smem_addr(&ctrl->never), 1);
@@ -1399,13 +1447,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const uint32_t smem_base = ptx::smem_addr(smem);
 
     if (warp == 0) {
-        if (lane == 0) pair_producer<kKind, kPairs>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
+        if (lane == 0) pair_producer<kKind, kPairs, kWide>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
     } else if (warp == PAIR_MMA_WARP) {
-        if (leader) pair_mma<kKind, kPairs>(p, smem_base, ctrl, tmem_base, rank, lane, wc);
+        if (leader) pair_mma<kKind, kPairs, kWide>(p, smem_base, ctrl, tmem_base, rank, lane, wc);
     } else if (warp == PAIR_WAITER_WARP) {
-        if (leader) pair_waiter<kKind, kPairs>(p, ctrl, lane, wc);
+        if (leader) pair_waiter<kKind, kPairs, kWide>(p, ctrl, lane, wc);
     } else {
-        pair_epilogue<kKind, kPairs>(p, &tmap_c, ctrl, tmem_base, smem_base + PAIR_STAGES * PAIR_STAGE_BYTES,
+        pair_epilogue<kKind, kPairs, kWide>(p, &tmap_c, ctrl, tmem_base, smem_base + PAIR_STAGES * PAIR_STAGE_BYTES,
                                      rank, warp, lane, wc);
     }
 
@@ -1484,7 +1532,7 @@ bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
 
 // Co-resident clusters of the pair kernel (clusters of 2 * kPairs CTAs) on the
 // current device (0 if the kernel cannot run), cached per device and kind.
-template <int kKind, int kPairs>
+template <int kKind, int kPairs, int kWide = 1>
 int pair_clusters()
 {
     constexpr int kMaxDevices = 64;
@@ -1494,7 +1542,7 @@ int pair_clusters()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     std::call_once(once[dev], [dev] {
         int n = 0;
-        if (cudaFuncSetAttribute(umma_pair_kernel<kKind, kPairs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(umma_pair_kernel<kKind, kPairs, kWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PAIR_SMEM_BYTES) == cudaSuccess) {
             int sms = 0;
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1505,11 +1553,11 @@ int pair_clusters()
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % (2 * kPairs)));
-            cfg.blockDim = dim3(PAIR_THREADS);
+            cfg.blockDim = dim3(pair_threads<kWide>());
             cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, umma_pair_kernel<kKind, kPairs>, &cfg) != cudaSuccess) n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, umma_pair_kernel<kKind, kPairs, kWide>, &cfg) != cudaSuccess) n = 0;
         }
         cudaGetLastError();  // a failed query leaves no sticky error behind
         cached[dev] = n;
@@ -1519,11 +1567,11 @@ int pair_clusters()
 
 // p.tiles_m / p.tiles_n count 256-row bands and supertile columns (256 * kPairs
 // columns each).
-template <int kKind, int kPairs>
+template <int kKind, int kPairs, int kWide = 1>
 bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const Params &p,
                  cudaStream_t stream)
 {
-    const int clusters = pair_clusters<kKind, kPairs>();
+    const int clusters = pair_clusters<kKind, kPairs, kWide>();
     if (clusters <= 0) return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
     const int64_t n = tiles < clusters ? tiles : clusters;
@@ -1534,12 +1582,12 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * kPairs * n));
-    cfg.blockDim = dim3(PAIR_THREADS);
+    cfg.blockDim = dim3(pair_threads<kWide>());
     cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kPairs>, ma, mb, mc, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kPairs, kWide>, ma, mb, mc, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -1629,7 +1677,7 @@ int cluster_capacity(int size)
 // Tile configuration of one call: the CTA-pair kernel (256 x 256 tiles), the
 // persistent single-CTA kernel (128 x bn tiles) or split-K over S CTAs of a
 // cluster (128 x bn tiles).
-enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3, kVariantQuad = 4 };
+enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3, kVariantQuad = 4, kVariantWide = 5 };
 struct UmmaConfig {
     int variant;
     int bn;
@@ -1676,6 +1724,13 @@ UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok, bool x2_ok
     // receives 32 KB per stage, and the shared ring couples the two pairs.
     // It stays reachable through dgemm_tune_next.)
     (void)x2_ok;
+    // a full wave (one per CTA pair) of 256 x 512 tiles or more: the wide pair
+    // tile, a quarter fewer operand bytes per flop into each SM (8192 x 8192 x
+    // 4096: TF32 998 vs 955 TFLOP/s, FP16 1844 vs 1817; 4096^3 TF32 852 vs
+    // 801); fewer: its single accumulator leaves too few tiles to hide the
+    // epilogue behind
+    const int64_t wide_tiles = ((p.M + PAIR_BM - 1) / PAIR_BM) * ((p.N + 2 * BN - 1) / (2 * BN));
+    if (pair_ok && p.M > BM && wide_tiles >= sm_count / 2) return {kVariantWide, BN, 1};
     if (tiles256 * 2 > sm_count) return {pair_ok && p.M > BM ? kVariantPair : kVariantSingle, BN, 1};
     const double kb_mma_us = 0.33 / 256.0;          // per column of bn, one K block
     const double sm_bytes_per_us = 75e3;            // 75 GB/s
@@ -1735,7 +1790,7 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorM
 template <int kKind>
 const char *variant_name(int variant, int bn = BN, int split = 1)
 {
-    static std::string names[3 + 9 * 9];
+    static std::string names[4 + 9 * 9];
     static std::once_flag once;
     std::call_once(once, [] {
         using T = Traits<kKind>;
@@ -1745,6 +1800,7 @@ const char *variant_name(int variant, int bn = BN, int split = 1)
         const std::string base = std::string("umma_") + kind;
         names[0] = base + "_pair_256x256x" + bk + "_tma";
         names[2 + 9 * 9] = base + "_pair_x2_256x512x" + bk + "_tma";
+        names[3 + 9 * 9] = base + "_pair_256x512x" + bk + "_tma";
         names[1] = base + "_128x256x" + bk + (kKind == kTF32 ? "_cpasync" : "_ldst");
         for (int w = 1; w <= 8; ++w) {
             const std::string tile = "128x" + std::to_string(32 * w) + "x" + bk;
@@ -1755,6 +1811,7 @@ const char *variant_name(int variant, int bn = BN, int split = 1)
     });
     if (variant == kVariantPair) return names[0].c_str();
     if (variant == kVariantQuad) return names[2 + 9 * 9].c_str();
+    if (variant == kVariantWide) return names[3 + 9 * 9].c_str();
     if (variant == kVariantAuto) return names[1].c_str();  // the non-TMA kernel
     const int w = bn / 32, S = variant == kVariantSplit ? split : 1;
     return names[2 + w * 9 + S].c_str();
@@ -1781,7 +1838,7 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
 {
     UmmaConfig cfg = t_tune;
     t_tune = UmmaConfig{kVariantAuto, BN, 1};
-    if (((cfg.variant == kVariantPair || cfg.variant == kVariantQuad) && !mb_pair) ||
+    if (((cfg.variant == kVariantPair || cfg.variant == kVariantQuad || cfg.variant == kVariantWide) && !mb_pair) ||
         cfg.bn % bn_step<kKind>() != 0)
         cfg.variant = kVariantAuto;
     if (cfg.variant == kVariantQuad && !ma_x2) cfg.variant = kVariantPair;
@@ -1792,9 +1849,16 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
     if (cfg.variant == kVariantAuto)
         cfg = choose_config<kKind>(p0, dev.sm_count, mb_pair != nullptr, ma_x2 != nullptr);
     Params p = p0;
-    if (cfg.variant == kVariantPair || cfg.variant == kVariantQuad) {
+    if (cfg.variant == kVariantPair || cfg.variant == kVariantQuad || cfg.variant == kVariantWide) {
         p.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
         p.b3d = pair3d;
+        if (cfg.variant == kVariantWide) {
+            Params w = p;
+            w.bn = 2 * BN;  // 256 x 512 pair tiles
+            w.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);
+            if (w.bn % box_cols<kKind>() != 0) w.tma_store = 0;
+            if (launch_pair<kKind, 1, 2>(ma, *mb_pair, mc, w, stream)) return variant_name<kKind>(kVariantWide);
+        }
         if (cfg.variant == kVariantQuad) {
             Params q = p;
             q.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);  // 256 x 512 supertiles
@@ -1919,7 +1983,7 @@ const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, 
 
 int umma_tune_next(int variant, int bn, int split)
 {
-    if (variant < kVariantAuto || variant > kVariantQuad) return DGEMM_ERR_INVALID_ARG;
+    if (variant < kVariantAuto || variant > kVariantWide) return DGEMM_ERR_INVALID_ARG;
     if ((variant == kVariantSingle || variant == kVariantSplit) && (bn < 32 || bn > BN || bn % 32 != 0))
         return DGEMM_ERR_INVALID_ARG;
     if (variant == kVariantSplit && (split < 2 || split > 8)) return DGEMM_ERR_INVALID_ARG;

@@ -37,7 +37,8 @@ KINDS = {
 def configs(step: int, sms: int, M: int, N: int):
     """Every (variant, bn, split) worth timing: the pair kernel, and for each
     tile width bn the single-CTA kernel and the splits that fit one wave."""
-    out = [(dg.TUNE_AUTO, 256, 1), (dg.TUNE_PAIR, 256, 1), (dg.TUNE_PAIR_X2, 256, 1)]
+    out = [(dg.TUNE_AUTO, 256, 1), (dg.TUNE_PAIR, 256, 1), (dg.TUNE_PAIR_X2, 256, 1),
+           (dg.TUNE_PAIR_WIDE, 256, 1)]
     tiles_m = (M + 127) // 128
     for bn in range(256, 31, -step):
         out.append((dg.TUNE_SINGLE, bn, 1))

@@ -254,7 +254,9 @@ int dgemm_test_inject_stall(uint64_t wait_limit_ns);
  *           2: one CTA per 128 x bn tile, persistent grid;
  *           3: split-K, `split` CTAs of a cluster per 128 x bn tile;
  *           4: two CTA pairs per cluster on a 256 x 512 supertile, the
- *              pairs sharing each A tile through TMA multicast.
+ *              pairs sharing each A tile through TMA multicast;
+ *           5: CTA pair, 256 x 512 output tiles (one 512-column
+ *              accumulator per CTA).
  *   bn:    tile width for variants 2 and 3: 32..256 in steps of 32; the
  *          NN 16-bit calls need a multiple of 64.  Ignored otherwise.
  *   split: 2..8 for variant 3 (lowered to the number of K blocks when K is

@@ -318,6 +318,36 @@ def test_pair_x2_integers_bit_exact(path):
     assert np.array_equal(got.double().numpy(), ref)
 
 
+@pytest.mark.parametrize("path", parity.TC_PATHS)
+@pytest.mark.parametrize("shape", [(300, 520, 264), (520, 1000, 200), (1000, 768, 520), (257, 1536, 64),
+                                   (129, 300, 40)])
+def test_pair_wide_kernel(path, shape):
+    import dense_gemm_09_gb300 as dg
+    # 256 x 512 pair tiles (two N = 256 MMAs per step, one 512-column
+    # accumulator, eight epilogue warps); N not a multiple of 512 leaves the
+    # tile's second half partly (1000) or wholly (300, 520) outside C
+    M, N, K = shape
+    if path.endswith("_nn") and N % 8:
+        N += 8 - N % 8  # a 16-bit NN B's pitch (N) must be a 16-byte multiple for TMA
+    A, B, C = parity.host_operands(path, M, N, K, seed=3 * M + N)
+    dg.tune_next(dg.TUNE_PAIR_WIDE)
+    got, _, _ = parity.run(path, A, B, C, 1.25, -0.5)
+    assert "_pair_256x512x" in dg.last_kernel(), dg.last_kernel()
+    assert parity.worst_ratio(path, got, A, B, C, 1.25, -0.5) <= 1.0
+
+
+@pytest.mark.parametrize("path", ["tf32", "f16_tn", "bf16_nn"])
+def test_pair_wide_integers_bit_exact(path):
+    import dense_gemm_09_gb300 as dg
+    # several tiles per pair (both accumulator phases), exact integer sums
+    A, B, C = parity.host_operands(path, 2048, 3072, 256, seed=9, dist="int")
+    dg.tune_next(dg.TUNE_PAIR_WIDE)
+    got, _, _ = parity.run(path, A, B, C, 1.0, 1.0)
+    assert "_pair_256x512x" in dg.last_kernel()
+    ref, _ = parity.reference(path, A, B, C, 1.0, 1.0)
+    assert np.array_equal(got.double().numpy(), ref)
+
+
 # Few output tiles and a long K: the split-K kernel (a cluster of S CTAs per
 # tile, partials reduced in distributed shared memory).
 SPLITK_CASES = [
