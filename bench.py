@@ -40,9 +40,9 @@ M = N = 8192
 K = 4096
 FLOPS = 2.0 * M * N * K
 PATHS = ("f32_simt", "tf32", "f16_tn")
-# profiling only: gemm_tf32_ws, whose operands TMA cannot load are repacked
-# into a workspace first (the ragged 8191 x 8193 x 4095 workload)
-EXTRA_PATHS = ("tf32_ws",)
+# profiling only: gemm_tf32_ws / gemm_f32_ws, which copy operands with odd
+# pitches into a workspace first (the ragged 8191 x 8193 x 4095 workload)
+EXTRA_PATHS = ("tf32_ws", "f32_ws")
 
 # Peaks (TFLOP/s).  FP32 SIMT: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz.
 SM_COUNT_NOMINAL = 152
@@ -63,11 +63,12 @@ def _peaks():
         src = "measured"
     return {"f16_tn": bf16, "tf32": bf16 * NOMINAL_TF32_OVER_BF16, "tf32_ws": bf16 * NOMINAL_TF32_OVER_BF16,
             "f32_simt": SM_COUNT_NOMINAL * 128 * 2 * SM_MAX_MHZ_NOMINAL * 1e6 / 1e12,
+            "f32_ws": SM_COUNT_NOMINAL * 128 * 2 * SM_MAX_MHZ_NOMINAL * 1e6 / 1e12,
             "source": src, "hbm_gbs": hbm, "bf16_sustained": bf16_sus}
 
 
 # Targets' denominators as recorded with the workload definition (datasheet-class).
-DATASHEET = {"f16_tn": 2250.0, "tf32": 1100.0, "tf32_ws": 1100.0, "f32_simt": 77.5}
+DATASHEET = {"f16_tn": 2250.0, "tf32": 1100.0, "tf32_ws": 1100.0, "f32_simt": 77.5, "f32_ws": 77.5}
 
 
 class ClockSampler:
@@ -196,22 +197,25 @@ def run_ours(args):
 
     # operands: one seeded problem per rank (replicas, weak scaling)
     ops = {}
-    if any(p in ("f32_simt", "tf32", "tf32_ws") for p in paths_run):
+    if any(p in ("f32_simt", "tf32", "tf32_ws", "f32_ws") for p in paths_run):
         w = si.Workload("bench_f32", "f32", Mx, Nx, Kx, 1.0, 0.0, "uniform", c_zero=True)
         Ah, Bh, _ = si.make(w, seed=rank, pin=True)
         f32 = (Ah, Bh, Ah.to(dev), Bh.to(dev), torch.zeros((Mx, Nx), dtype=torch.float32, device=dev))
-        ops["f32_simt"] = ops["tf32"] = ops["tf32_ws"] = f32
+        ops["f32_simt"] = ops["tf32"] = ops["tf32_ws"] = ops["f32_ws"] = f32
     if "f16_tn" in paths_run:
         w = si.Workload("bench_f16", "f16_tn", Mx, Nx, Kx, 1.0, 0.0, "normal_sqrtk", c_zero=True)
         Ah, Bh, _ = si.make(w, seed=rank, pin=True)
         ops["f16_tn"] = (Ah, Bh, Ah.to(dev), Bh.to(dev),
                          torch.zeros((Mx, Nx), dtype=torch.float16, device=dev))
     fns = {"f32_simt": dg.gemm_f32, "tf32": dg.gemm_tf32, "f16_tn": dg.gemm_f16_tn}
-    if "tf32_ws" in paths_run:
-        nws = dg.tf32_workspace_bytes(ops["tf32_ws"][2], ops["tf32_ws"][3])
+    if "tf32_ws" in paths_run or "f32_ws" in paths_run:
+        wp = "tf32_ws" if "tf32_ws" in paths_run else "f32_ws"
+        nws = dg.tf32_workspace_bytes(ops[wp][2], ops[wp][3])
         ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev) if nws else None
         fns["tf32_ws"] = lambda A, B, C, a, b, stream: dg.gemm_tf32_ws(A, B, C, a, b, workspace=ws,
                                                                        stream=stream)
+        fns["f32_ws"] = lambda A, B, C, a, b, stream: dg.gemm_f32_ws(A, B, C, a, b, workspace=ws,
+                                                                     stream=stream)
     # L2 flush: write 512 MiB (evicts the operands), then read another 256 MiB
     # so that the lines left in L2 are clean -- otherwise the timed kernel
     # would start by writing back the flush's dirty lines.
@@ -332,13 +336,14 @@ def run_ours(args):
                     "frac_of_datasheet": round(tf / DATASHEET[p], 4)}
     dominant = max(paths_run, key=lambda p: paths[p]["ms"])
     dom = paths[dominant]
-    kfile = "sgemm_simt.cu" if dominant == "f32_simt" else "umma_gemm.cu"
+    simt = dominant in ("f32_simt", "f32_ws")
+    kfile = "sgemm_simt.cu" if simt else "umma_gemm.cu"
     roofline = {"kernel": dom["kernel"],
-                "bound": "alu" if dominant == "f32_simt" else "tensor",
+                "bound": "alu" if simt else "tensor",
                 "achieved": dom["tflops"], "peak": dom["peak_tflops"], "unit": "TFLOP/s",
                 "frac": dom["frac_of_peak"],
                 "peak_source": ("derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz"
-                                if dominant == "f32_simt" else
+                                if simt else
                                 peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)" +
                                 (" x nominal tf32/bf16 ratio 1.1/2.25" if dominant.startswith("tf32") else "")),
                 "traffic": _traffic_for(kfile, dom["kernel"], (Mx, Nx, Kx))}

@@ -74,6 +74,8 @@ def lib():
         L.dgemm_tune_next.restype = ci
         L.gemm_tf32_ws.argtypes = sig[:11] + [vp, i64, vp]
         L.gemm_tf32_ws.restype = ci
+        L.gemm_f32_ws.argtypes = sig[:11] + [vp, i64, vp]
+        L.gemm_f32_ws.restype = ci
         L.gemm_tf32_workspace_bytes.argtypes = [i64, i64, i64, vp, i64, vp, i64]
         L.gemm_tf32_workspace_bytes.restype = i64
         L.gemm_tf32_noalloc.argtypes = sig
@@ -177,10 +179,7 @@ def tf32_workspace_bytes(A, B) -> int:
     return int(n)
 
 
-def gemm_tf32_ws(A, B, C, alpha: float = 1.0, beta: float = 0.0, workspace=None, stream=None):
-    """gemm_tf32 for operands whose base or row pitch TMA cannot load: they
-    are copied into ``workspace`` (a CUDA tensor of at least
-    tf32_workspace_bytes(A, B) bytes, 16-byte aligned) first."""
+def _ws_call(name, A, B, C, alpha, beta, workspace, stream):
     pa, lda = _mat(A, "A", torch.float32)
     pb, ldb = _mat(B, "B", torch.float32)
     pc, ldc = _mat(C, "C", torch.float32)
@@ -193,11 +192,25 @@ def gemm_tf32_ws(A, B, C, alpha: float = 1.0, beta: float = 0.0, workspace=None,
         if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
             raise ValueError("workspace must be a CUDA tensor")
         pw, nw = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    st = lib().gemm_tf32_ws(M, N, K, float(alpha), pa, lda, pb, ldb, float(beta), pc, ldc,
-                            pw or None, nw, _stream(stream))
+    st = getattr(lib(), name)(M, N, K, float(alpha), pa, lda, pb, ldb, float(beta), pc, ldc,
+                              pw or None, nw, _stream(stream))
     if st != OK:
-        raise DgemmError(st, "gemm_tf32_ws")
+        raise DgemmError(st, name)
     return C
+
+
+def gemm_tf32_ws(A, B, C, alpha: float = 1.0, beta: float = 0.0, workspace=None, stream=None):
+    """gemm_tf32 for operands whose base or row pitch TMA cannot load: they
+    are copied into ``workspace`` (a CUDA tensor of at least
+    tf32_workspace_bytes(A, B) bytes, 16-byte aligned) first."""
+    return _ws_call("gemm_tf32_ws", A, B, C, alpha, beta, workspace, stream)
+
+
+def gemm_f32_ws(A, B, C, alpha: float = 1.0, beta: float = 0.0, workspace=None, stream=None):
+    """gemm_f32 with the same workspace: a B whose base or row pitch is not a
+    16-byte multiple is copied first, so the SIMT kernel loads it in 16-byte
+    pieces."""
+    return _ws_call("gemm_f32_ws", A, B, C, alpha, beta, workspace, stream)
 
 
 # Bytes of the library's fixed scratch behind gemm_tf32_noalloc (see

@@ -230,6 +230,29 @@ extern "C" int gemm_tf32_ws(int64_t M, int64_t N, int64_t K, float alpha, const 
                               r.b ? r.ldb : N));
 }
 
+extern "C" int gemm_f32_ws(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                           const float *B, int64_t ldb, float beta, float *C, int64_t ldc, void *workspace,
+                           int64_t workspace_bytes, cudaStream_t stream)
+{
+    int st = validate(M, N, K, alpha, A, lda, B, ldb, N, C, ldc);
+    if (st != DGEMM_OK || M == 0 || N == 0) return st;
+    DeviceInfo dev;
+    if ((st = check_device(dev)) != DGEMM_OK) return st;
+    if (K == 0 || alpha == 0.f) return finish(launch_scale_f32(M, N, beta, C, ldc, stream));
+    // only B is copied: the SIMT kernel loads A element by element whatever
+    // its alignment, and B in 16-byte pieces when its rows allow
+    const Tf32Repack r = plan_tf32_repack(M, N, K, A, lda, B, ldb);
+    if (r.bytes < 0) return DGEMM_ERR_INVALID_ARG;
+    if (r.b) {
+        if (!workspace || workspace_bytes < r.bytes || !aligned16(workspace)) return DGEMM_ERR_INVALID_ARG;
+        float *wb = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + r.off_b);
+        if (!launch_repack_f32(B, K, N, ldb, wb, r.ldb, stream, dev)) return DGEMM_ERR_LAUNCH;
+        B = wb;
+        ldb = r.ldb;
+    }
+    return finish(launch_sgemm_simt(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev));
+}
+
 extern "C" const char *dgemm_status_string(int status)
 {
     switch (status) {

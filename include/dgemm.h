@@ -138,6 +138,23 @@ int gemm_tf32_ws(int64_t M, int64_t N, int64_t K, float alpha,
 int64_t gemm_tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                                   const float *B, int64_t ldb);
 
+/*
+ * gemm_f32_ws -- gemm_f32 with the workspace of gemm_tf32_ws (same layout,
+ * same size: gemm_tf32_workspace_bytes, of which it uses only B's part).
+ * When B's base or row pitch is not a 16-byte multiple (e.g. ldb = N = 8193),
+ * B is first copied bit for bit into the workspace with a padded pitch, so
+ * that the SIMT kernel loads it in 16-byte pieces instead of 4-byte ones; A
+ * is loaded element by element in either case and is not copied.  Results
+ * are the same as gemm_f32 on the same values.  Workspace rules and errors
+ * as gemm_tf32_ws; the call allocates nothing.
+ * Source: the operation of gemm_f32 ("SGEMM CUDA代码学习", "第 5 步":
+ * 16-byte asynchronous copies need 16-byte aligned addresses).
+ */
+int gemm_f32_ws(int64_t M, int64_t N, int64_t K, float alpha,
+                const float *A, int64_t lda, const float *B, int64_t ldb,
+                float beta, float *C, int64_t ldc,
+                void *workspace, int64_t workspace_bytes, cudaStream_t stream);
+
 /* Size of the fixed scratch array behind gemm_tf32_noalloc (64 MiB). */
 #define DGEMM_NOALLOC_SCRATCH_BYTES (64LL * 1024 * 1024)
 

@@ -131,6 +131,7 @@ def test_tune_next_validates_on_host(L):
 ])
 def test_tf32_ws_invalid_arguments_rejected_on_host(L, args):
     assert L.gemm_tf32_ws(*args, P, 1 << 20, None) == 1
+    assert L.gemm_f32_ws(*args, P, 1 << 20, None) == 1
 
 
 def test_tf32_ws_empty_problem_returns_ok_without_device(L):

@@ -125,3 +125,44 @@ def test_ws_ragged_workload_full_size():
     assert dg.device_status() == dg.OK
     assert "_pair_" in dg.last_kernel()
     assert parity.sampled_check("tf32", dC, A, B, C, w.alpha, w.beta) <= 1.0
+
+
+# gemm_f32_ws: the SIMT path with the same workspace; only B is copied.
+F32_CASES = [
+    (129, 257, 301, (0, 0), (0, 0)),      # odd N: B's pitch off 16 bytes
+    (300, 520, 1000, (0, 3), (0, 0)),     # B pitch 523
+    (300, 520, 1000, (0, 0), (0, 2)),     # B base off 16 bytes
+    (1000, 1100, 513, (2, 2), (3, 1)),
+]
+
+
+@pytest.mark.parametrize("M,N,K,pad,offset", F32_CASES)
+def test_f32_ws_matches_oracle_and_plain_call(M, N, K, pad, offset):
+    import dense_gemm_09_gb300 as dg
+    A, B, C = parity.host_operands("f32", M, N, K, seed=5 * M + N)
+    dA, _ = parity.to_device_padded(A, pad[0], offset_elems=offset[0])
+    dB, _ = parity.to_device_padded(B, pad[1], offset_elems=offset[1])
+    n, ws = _workspace(dg, dA, dB)
+    assert n > 0
+    got = C.cuda()
+    dg.gemm_f32_ws(dA, dB, got, 1.5, -0.25, workspace=ws)
+    torch.cuda.synchronize()
+    assert dg.last_kernel().endswith("cpasync16"), dg.last_kernel()  # B now loads in 16-byte pieces
+    assert parity.worst_ratio("f32", got.cpu(), A, B, C, 1.5, -0.25) <= 1.0
+    # the same FP32 FMAs in the same order as the plain call on the same values
+    want = C.cuda()
+    dg.gemm_f32(dA, dB, want, 1.5, -0.25)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+
+
+def test_f32_ws_rejects_a_missing_workspace():
+    import dense_gemm_09_gb300 as dg
+    A, B, C = parity.host_operands("f32", 64, 77, 40, seed=1)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    assert dg.tf32_workspace_bytes(dA, dB) > 0
+    with pytest.raises(dg.DgemmError) as e:
+        dg.gemm_f32_ws(dA, dB, dC, 1.0, 0.0, workspace=None)
+    assert e.value.status == dg.ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.equal(dC.cpu(), C)
