@@ -1724,13 +1724,18 @@ UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok, bool x2_ok
     // receives 32 KB per stage, and the shared ring couples the two pairs.
     // It stays reachable through dgemm_tune_next.)
     (void)x2_ok;
-    // a full wave (one per CTA pair) of 256 x 512 tiles or more: the wide pair
-    // tile, a quarter fewer operand bytes per flop into each SM (8192 x 8192 x
-    // 4096: TF32 998 vs 955 TFLOP/s, FP16 1844 vs 1817; 4096^3 TF32 852 vs
-    // 801); fewer: its single accumulator leaves too few tiles to hide the
-    // epilogue behind
-    const int64_t wide_tiles = ((p.M + PAIR_BM - 1) / PAIR_BM) * ((p.N + 2 * BN - 1) / (2 * BN));
-    if (pair_ok && p.M > BM && wide_tiles >= sm_count / 2) return {kVariantWide, BN, 1};
+    // 256 x 512 pair tiles carry a quarter fewer operand bytes per flop into
+    // each SM, worth ~3 % per tile (8192 x 8192 x 4096: TF32 1024 vs 994
+    // TFLOP/s), but a wide tile takes twice as long, so it pays only when the
+    // rounds of tiles over the CTA pairs come out no worse: taken when
+    // 2 x 0.97 x rounds(wide) < rounds(256 x 256) (8192 x 8448 x 4096: 14
+    // rounds of pair tiles against 8 of wide ones, TF32 1008 vs 917)
+    const int64_t pairs = sm_count / 2;
+    const int64_t bands = (p.M + PAIR_BM - 1) / PAIR_BM;
+    const int64_t rounds_pair = (bands * ((p.N + BN - 1) / BN) + pairs - 1) / pairs;
+    const int64_t rounds_wide = (bands * ((p.N + 2 * BN - 1) / (2 * BN)) + pairs - 1) / pairs;
+    if (pair_ok && p.M > BM && rounds_wide >= 1 && 2.0 * 0.97 * rounds_wide < rounds_pair)
+        return {kVariantWide, BN, 1};
     if (tiles256 * 2 > sm_count) return {pair_ok && p.M > BM ? kVariantPair : kVariantSingle, BN, 1};
     const double kb_mma_us = 0.33 / 256.0;          // per column of bn, one K block
     const double sm_bytes_per_us = 75e3;            // 75 GB/s
