@@ -207,6 +207,15 @@ struct Params {
     // (column group of 128 bytes x BK rows x 128 / kNBox groups) instead of
     // 128 / kNBox 2-D boxes
     int b3d;
+    // CTA-pair kernel, stream-K: tiles [0, sk_tiles) of the tile order are
+    // cut along K into one contiguous range of K blocks per pair (0 = every
+    // tile whole).  A pair that ends inside a tile leaves its raw partial
+    // accumulator in its slot of sk_work and stamps sk_flags with sk_gen; the
+    // pair that continues the tile loads it into TMEM and keeps accumulating.
+    int64_t sk_tiles;
+    float *sk_work;
+    uint64_t *sk_flags;
+    uint64_t sk_gen;
 };
 
 // The instruction descriptor with its N field (bits 17-22, N >> 3) set to n.
@@ -1151,6 +1160,7 @@ struct PairCtrl {
     uint64_t empty[PAIR_STAGES];  // the pair's MMAs have read this stage
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
+    uint64_t acc_ready;  // stream-K: every epilogue warp has loaded its part of a partial
     uint64_t mma_done;
     uint64_t never;  // test hook: a barrier nothing arrives at
     WaitCtl wait;
@@ -1195,6 +1205,191 @@ struct PairShape {
     static constexpr int kAccCols = BN * kWide;
 };
 
+// ---- stream-K tail
+//
+// With T tiles on P pairs and T mod P = r != 0, whole tiles dealt round-robin
+// leave r pairs busy in the last round and P - r idle.  Instead the first
+// P + r tiles of the tile order are cut along K: their (P + r) x num_kb K
+// blocks are dealt in P contiguous ranges, one per pair (at least num_kb
+// blocks each, so no range lies strictly inside one tile and each tile is
+// cut at most once); the remaining (T / P - 1) x P tiles go round-robin.
+// A pair walks its range from its last tile back to its first:
+//   * the head [0, k) of its last tile (when the range ends inside it) comes
+//     first; its raw f32 accumulator goes to the pair's slot of sk_work
+//     ("publish") and each epilogue warp stamps its flag with sk_gen;
+//   * whole tiles in between are ordinary;
+//   * the tail [k, num_kb) of its first tile comes last: each epilogue warp
+//     waits for the previous pair's flag, loads that partial into TMEM
+//     ("init"), and the MMAs accumulate onto it.
+// The MMAs of a cut tile therefore run in exactly the order of an uncut one,
+// so the result is bit-identical to the round-robin schedule.  A partial is
+// published at the start of a pair's work and consumed at the end of the
+// next pair's, so the wait is normally already satisfied.
+struct Unit {
+    int64_t t;       // tile in tile order
+    int64_t k0, k1;  // K blocks [k0, k1)
+    bool init;       // start from the previous pair's partial (k0 > 0)
+    bool publish;    // leave the partial for the next pair (k1 < num_kb)
+};
+
+struct WorkIter {
+    int64_t t_sk, t_sk_first, b, e;  // stream-K: next tile (descending), first tile, K-block range
+    int64_t t_dp, dt_dp, tiles;      // round-robin: next tile, stride, tile count
+
+    __device__ __forceinline__ WorkIter(const Params &p, int64_t cluster, int64_t clusters)
+    {
+        tiles = p.tiles_m * p.tiles_n;
+        if (p.sk_tiles > 0) {
+            const int64_t blocks = p.sk_tiles * p.num_kb;
+            b = cluster * blocks / clusters;
+            e = (cluster + 1) * blocks / clusters;
+            t_sk_first = b / p.num_kb;
+            t_sk = (e - 1) / p.num_kb;
+        } else {
+            b = e = 0;
+            t_sk_first = 0;
+            t_sk = -1;
+        }
+        t_dp = p.sk_tiles + cluster;
+        dt_dp = clusters;
+    }
+
+    // whether the unit after the current one is the "init" tail
+    __device__ __forceinline__ bool next_is_init(const Params &p) const
+    {
+        return t_sk == t_sk_first && b > t_sk_first * p.num_kb;
+    }
+
+    __device__ __forceinline__ bool next(const Params &p, Unit &u)
+    {
+        if (t_sk >= t_sk_first) {
+            const int64_t base = t_sk * p.num_kb;
+            u.t = t_sk;
+            u.k0 = b > base ? b - base : 0;
+            u.k1 = e < base + p.num_kb ? e - base : p.num_kb;
+            u.init = u.k0 > 0;
+            u.publish = u.k1 < p.num_kb;
+            --t_sk;
+            return true;
+        }
+        if (t_dp < tiles) {
+            u.t = t_dp;
+            u.k0 = 0;
+            u.k1 = p.num_kb;
+            u.init = u.publish = false;
+            t_dp += dt_dp;
+            return true;
+        }
+        return false;
+    }
+};
+
+// Partials: per pair slot, CTA half and epilogue warp (8 slots; the 256-wide
+// tiles use 4) a region of 32 rows x 256 columns of f32 = 32 KB, laid out
+// [32-column chunk][column quad][row] in 16-byte units so that each warp
+// access is 512 contiguous bytes.  One flag per region.
+constexpr int SK_WARP_SLOTS = 8;
+constexpr int64_t SK_REGION_FLOATS = 32 * 256;
+
+__device__ __forceinline__ int64_t sk_region(int64_t slot, uint32_t half, int w)
+{
+    return (slot * 2 + half) * SK_WARP_SLOTS + w;
+}
+
+// Store this warp's 32 rows x cols accumulator columns (cols a multiple of 32)
+// to its region.  The caller may release TMEM afterwards, then stamps the
+// flag with sk_flag().
+__device__ __forceinline__ void sk_publish(const Params &p, uint32_t taddr, int cols, int64_t region,
+                                          int lane)
+{
+    float4 *dst = reinterpret_cast<float4 *>(p.sk_work + region * SK_REGION_FLOATS);
+#pragma unroll 1
+    for (int c = 0; c < cols / 32; ++c) {
+        uint32_t r[32];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            dst[(c * 8 + j) * 32 + lane] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                       __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+    }
+}
+
+// Stamp the region's flag once every lane's stores are visible (release).
+__device__ __forceinline__ void sk_flag(const Params &p, int64_t region, int lane)
+{
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) ptx::st_release_gpu_u64(p.sk_flags + region, p.sk_gen);
+}
+
+// If the region's partial is already published, pull its lines into L2 (the
+// warp is otherwise idle, waiting for an accumulator), so that sk_init's
+// loads do not go to HBM.
+__device__ __forceinline__ void sk_prefetch(const Params &p, int cols, int64_t region, int lane)
+{
+    const bool ready = ptx::ld_acquire_gpu_u64(p.sk_flags + region) == p.sk_gen;
+    if (!ready) return;
+    const char *base = reinterpret_cast<const char *>(p.sk_work + region * SK_REGION_FLOATS);
+    const int lines = cols * 32 * 4 / 128;  // 128-byte lines of the region in use
+    for (int l = lane; l < lines; l += 32) ptx::prefetch_l2(base + static_cast<int64_t>(l) * 128);
+}
+
+// Wait (bounded) for the region's flag to carry this launch's generation,
+// then load the partial into this warp's 32 TMEM lanes x BN columns, two
+// chunks in flight.  False on time-out or abort.
+__device__ __forceinline__ bool sk_init(const Params &p, uint32_t taddr, int64_t region, int lane, WaitCtl *wc)
+{
+    constexpr int kChunks = BN / 32;
+    static_assert(kChunks % 2 == 0, "chunks are loaded in pairs");
+    bool ok = true;
+    if (lane == 0) {
+        const uint64_t *flag = p.sk_flags + region;
+        if (ptx::ld_acquire_gpu_u64(flag) != p.sk_gen) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            for (;;) {
+                if (ptx::ld_acquire_gpu_u64(flag) == p.sk_gen) break;
+                if (aborted(wc)) {
+                    ok = false;
+                    break;
+                }
+                if (ptx::globaltimer_ns() - t0 > wc->limit_ns) {
+                    raise_abort(wc);
+                    ok = false;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+    }
+    if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return false;
+    (void)ptx::ld_acquire_gpu_u64(p.sk_flags + region);  // every lane acquires before its loads
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.sk_work + region * SK_REGION_FLOATS) + lane;
+    // chunks c and c + 1 in two register sets (L2 loads: written during this launch)
+    uint32_t ra[32], rb[32];
+    auto load = [&](uint32_t (&r)[32], int c) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 v = __ldcg(src + (c * 8 + j) * 32);
+            r[4 * j] = v.x;
+            r[4 * j + 1] = v.y;
+            r[4 * j + 2] = v.z;
+            r[4 * j + 3] = v.w;
+        }
+    };
+    load(ra, 0);
+#pragma unroll 1
+    for (int c = 0; c < kChunks; c += 2) {
+        load(rb, c + 1);
+        ptx::tmem_st_32x32b_x32(taddr + c * 32, ra);
+        if (c + 2 < kChunks) load(ra, c + 2);
+        ptx::tmem_st_32x32b_x32(taddr + (c + 1) * 32, rb);
+    }
+    ptx::tmem_st_wait();
+    return true;
+}
+
 template <int kKind, int kPairs, int kWide>
 __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
                                               const Params &p, uint32_t smem_base, PairCtrl *ctrl,
@@ -1205,16 +1400,17 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
     constexpr int kCtas = 2 * kPairs;
     constexpr int kRowsA = 128 / kPairs;  // A rows this CTA loads per stage
     constexpr uint16_t kHalfMask = kPairs == 1 ? 0x1 : 0x5;  // the even CTA of every pair
-    const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const int64_t cluster = blockIdx.x / kCtas, clusters = gridDim.x / kCtas;
     const uint32_t half = rank & 1u, pair = rank >> 1, leader = rank & ~1u;
     uint32_t stage = 0, phase = 0;
     uint32_t issued = 0, issued_phase = 0;
     bool ok = true;
-    for (int64_t t = cluster; ok && t < num_tiles; t += clusters) {
+    WorkIter it(p, cluster, clusters);
+    Unit u;
+    while (ok && it.next(p, u)) {
         int64_t m0, n0;
-        pair_tile<kPairs>(t, p, rank, m0, n0);
-        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+        pair_tile<kPairs>(u.t, p, rank, m0, n0);
+        for (int64_t kb = u.k0; kb < u.k1; ++kb) {
             if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
                 ok = false;
                 break;
@@ -1273,12 +1469,13 @@ template <int kKind, int kPairs, int kWide>
 __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int lane, WaitCtl *wc)
 {
     using S = PairShape<kWide>;
-    const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
     uint32_t stage = 0, phase = 0;
     bool abort = false;
-    for (int64_t t = cluster; t < num_tiles; t += clusters) {
-        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+    WorkIter it(p, cluster, clusters);
+    Unit u;
+    while (it.next(p, u)) {
+        for (int64_t kb = u.k0; kb < u.k1; ++kb) {
             if (!abort) {
                 bool ok = true;
                 if (lane == 0) ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->full[stage]), phase, wc);
@@ -1306,22 +1503,27 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
     using S = PairShape<kWide>;
     constexpr uint16_t kAll = static_cast<uint16_t>((1u << (2 * kPairs)) - 1u);
     const uint16_t kPair = static_cast<uint16_t>(0x3u << rank);
-    const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
-    uint32_t stage = 0, acc = 0, acc_phase = 0;
+    uint32_t stage = 0, acc = 0, acc_phase = 0, ready_phase = 0;
     // test hook: wait on a barrier nothing arrives at, so the wait runs out
     bool ok = true;
     if (lane == 0 && p.inject_stall) ok = wait_bounded(ptx::smem_addr(&ctrl->never), 0, wc);
     bool abort = __shfl_sync(0xffffffffu, ok ? 0 : 1, 0) != 0;
-    for (int64_t t = cluster; t < num_tiles; t += clusters) {
+    WorkIter it(p, cluster, clusters);
+    Unit u;
+    while (it.next(p, u)) {
         if (!abort) {
             ok = true;
             if (lane == 0)
                 ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_empty[acc]), acc_phase ^ 1u, wc);
+            // stream-K: the epilogue warps load the previous pair's partial first
+            if (ok && lane == 0 && u.init) ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->acc_ready), ready_phase, wc);
             abort = __shfl_sync(0xffffffffu, ok ? 0 : 1, 0) != 0;
         }
+        if (u.init) ready_phase ^= 1u;
+        const uint32_t acc_first = u.init ? 1u : 0u;  // accumulate onto the loaded partial
         const uint32_t d_tmem = tmem_base + acc * S::kAccCols;
-        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+        for (int64_t kb = u.k0; kb < u.k1; ++kb) {
             abort = ptx::bar_red_or(1 + stage, PAIR_HANDOFF_THREADS, abort);
             if (!abort) {
                 ptx::tc_fence_after();
@@ -1339,7 +1541,7 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
                             else
                                 db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
                             ptx::umma_pair<kKind>(d_tmem + w * BN, da, db, pair_idesc<kKind>(),
-                                                  (kb | k) != 0 ? 1u : 0u);
+                                                  (kb != u.k0 || k != 0) ? 1u : acc_first);
                         }
                     }
                     ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), kAll);
@@ -1367,25 +1569,51 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap
                                               PairCtrl *ctrl, uint32_t tmem_base, uint32_t epi_smem,
                                               uint32_t rank, int warp, int lane, WaitCtl *wc)
 {
-    const int64_t num_tiles = p.tiles_m * p.tiles_n;
     const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
     const uint32_t quarter = static_cast<uint32_t>(warp & 3);
     const uint32_t leader = rank & ~1u;
     // kWide = 2: warps 2-5 drain columns 0-255, warps 7-10 columns 256-511
     const uint32_t colhalf = kWide == 2 && warp >= 7 ? 1u : 0u;
-    const uint32_t box = kWide == 2 ? epi_smem + static_cast<uint32_t>(warp - (warp >= 7 ? 3 : 2)) * EPI_BOX_BYTES
+    const int slot = kWide == 2 ? warp - (warp >= 7 ? 3 : 2) : warp - 2;  // 0..7 / 0..3
+    const uint32_t box = kWide == 2 ? epi_smem + static_cast<uint32_t>(slot) * EPI_BOX_BYTES
                                     : epi_smem + quarter * 2 * EPI_BOX_BYTES;
+    constexpr int kAccs = PairShape<kWide>::kAccs;
     uint32_t acc = 0, acc_phase = 0, nbox = 0;
-    for (int64_t t = cluster; t < num_tiles; t += clusters) {
+    WorkIter it(p, cluster, clusters);
+    Unit u;
+    while (it.next(p, u)) {
         int64_t m0, n0;
-        pair_tile<kPairs>(t, p, rank, m0, n0);
+        pair_tile<kPairs>(u.t, p, rank, m0, n0);
+        const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * PairShape<kWide>::kAccCols +
+                               colhalf * BN;
+        // Stream-K "init": load the previous pair's partial into the unit's
+        // accumulator before its MMAs.  With two accumulators it is done one
+        // unit ahead, while this unit's MMAs run: the next unit's accumulator
+        // was drained in the previous iteration.  With one, it waits for this
+        // unit (the accumulator is free only now); the lines are pulled into
+        // L2 a unit ahead instead.
+        bool init_now = kAccs == 1 && u.init;
+        uint32_t init_addr = taddr;
+        if (kAccs == 2 && it.next_is_init(p)) {
+            init_now = true;
+            init_addr = acc ? taddr - PairShape<kWide>::kAccCols : taddr + PairShape<kWide>::kAccCols;  // the other one
+        } else if (kAccs == 1 && it.next_is_init(p)) {
+            sk_prefetch(p, BN, sk_region(cluster - 1, rank & 1u, slot), lane);
+        }
+        if (init_now) {
+            if (!sk_init(p, init_addr, sk_region(cluster - 1, rank & 1u, slot), lane, wc)) break;
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_addr(&ctrl->acc_ready), leader));
+        }
         bool ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_full[acc]), acc_phase, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * PairShape<kWide>::kAccCols;
-        if constexpr (kWide == 2)
-            drain_rows<kKind, 1>(p, tmap_c, taddr + colhalf * BN, m0 + (rank & 1u) * 128 + quarter * 32,
+        if (u.publish)
+            sk_publish(p, taddr, BN, sk_region(cluster, rank & 1u, slot), lane);
+        else if constexpr (kWide == 2)
+            drain_rows<kKind, 1>(p, tmap_c, taddr, m0 + (rank & 1u) * 128 + quarter * 32,
                                  n0 + colhalf * BN, box, lane, nbox, BN);
         else
             drain_rows<kKind>(p, tmap_c, taddr, m0 + (rank & 1u) * 128 + quarter * 32, n0, box, lane, nbox);
@@ -1393,6 +1621,7 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap
         __syncwarp();
         if (lane == 0)
             ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_addr(&ctrl->tmem_empty[acc]), leader));
+        if (u.publish) sk_flag(p, sk_region(cluster, rank & 1u, slot), lane);  // after TMEM is released
         if (++acc == PairShape<kWide>::kAccs) {
             acc = 0;
             acc_phase ^= 1u;
@@ -1424,6 +1653,7 @@ __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
             ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_full[a]), 1);
             ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_empty[a]), 8 * kWide);  // epilogue warps x 2 CTAs
         }
+        ptx::mbar_init(ptx::smem_addr(&ctrl->acc_ready), 8 * kWide);
         ptx::mbar_init(ptx::smem_addr(&ctrl->mma_done), 1);
         ptx::mbar_init(ptx::smem_addr(&ctrl->never), 1);
         ctrl->wait.abort = 0;
@@ -1565,12 +1795,107 @@ int pair_clusters()
     return cached[dev];
 }
 
-// p.tiles_m / p.tiles_n count 256-row bands and supertile columns (256 * kPairs
-// columns each).
-template <int kKind, int kPairs, int kWide = 1>
-bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const Params &p,
-                 cudaStream_t stream)
+// ---- stream-K workspace
+//
+// One per device, allocated on the first stream-K launch and kept: a slot of
+// partial sums per CTA pair (2 halves x 8 warp regions x 32 KB = 512 KB;
+// 38 MB for 76 pairs) and one 64-bit flag per region.  Launches that use it
+// are ordered one after another, on whatever streams they come from, through
+// an event that each records and the next waits for; each launch stamps its
+// flags with a new generation, so flags left by earlier launches (or by an
+// aborted one) never match.  Stream-K is not used while the stream is being
+// captured into a graph (the graph would hold the shared workspace); the
+// round-robin schedule then runs, with bit-identical results.
+struct SkWorkspace {
+    std::mutex mu;
+    float *work = nullptr;
+    uint64_t *flags = nullptr;
+    int64_t slots = 0;
+    cudaEvent_t last = nullptr;
+    bool recorded = false;
+    bool failed = false;
+    uint64_t gen = 0;
+};
+
+SkWorkspace *sk_workspace(int dev)
 {
+    constexpr int kMaxDevices = 64;
+    static SkWorkspace ws[kMaxDevices];
+    return dev >= 0 && dev < kMaxDevices ? &ws[dev] : nullptr;
+}
+
+// Allocate the device's workspace for `slots` pairs (once; mu held).
+bool sk_ensure(SkWorkspace &w, int64_t slots, cudaStream_t stream)
+{
+    if (w.work) return w.slots >= slots;
+    if (w.failed) return false;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        slots = std::max<int64_t>(slots, sms / 2);  // every pair count this device can run
+    const size_t regions = static_cast<size_t>(slots) * 2 * SK_WARP_SLOTS;
+    void *work = nullptr, *flags = nullptr;
+    cudaEvent_t ev = nullptr;
+    if (cudaMalloc(&work, regions * SK_REGION_FLOATS * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(&flags, regions * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemsetAsync(flags, 0, regions * sizeof(uint64_t), stream) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        if (work) cudaFree(work);
+        if (flags) cudaFree(flags);
+        w.failed = true;
+        return false;
+    }
+    w.work = static_cast<float *>(work);
+    w.flags = static_cast<uint64_t *>(flags);
+    w.slots = slots;
+    w.last = ev;
+    return true;
+}
+
+bool stream_capturing(cudaStream_t stream)
+{
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) {
+        cudaGetLastError();
+        return true;  // cannot tell: take the schedule that needs no workspace
+    }
+    return st != cudaStreamCaptureStatusNone;
+}
+
+// Stream-K modes of the pair kernels (the `split` field of their tuning).
+enum { kSkAuto = 0, kSkOff = 1, kSkOn = 2 };
+// Estimated K-block time of one pair tile, 256 x 256 (us; x2 for 256 x 512):
+// ~8.4 MFLOP (FP16, BK = 64) or ~4.2 MFLOP (TF32, BK = 32) at a pair's share
+// of the measured rates (0.32 us for both on GB300).
+constexpr double kSkKbUs = 0.32;
+// Least estimated saving for a stream-K launch: the partials' round trip
+// (a 256 KB store per CTA, and a load that the continuing pair's MMAs wait
+// for) costs a few microseconds.
+constexpr double kSkMinSavedUs = 8.0;
+
+// Tiles of the stream-K region for T tiles on P pairs (0: whole tiles
+// round-robin): P + T mod P when the tiles outnumber the pairs and the idle
+// share of the last round is worth more than the partials cost.
+int64_t stream_k_tiles(int64_t tiles, int64_t pairs, int64_t num_kb, double kb_us, int mode)
+{
+    if (mode == kSkOff || pairs < 2 || tiles <= pairs) return 0;
+    const int64_t r = tiles % pairs;
+    if (mode == kSkOn) return pairs + r;
+    if (r == 0) return 0;
+    const double saved_us = (1.0 - static_cast<double>(r) / static_cast<double>(pairs)) *
+                            static_cast<double>(num_kb) * kb_us;
+    return saved_us > kSkMinSavedUs ? pairs + r : 0;
+}
+
+// p.tiles_m / p.tiles_n count 256-row bands and supertile columns (256 * kPairs
+// columns each).  sk_mode: kSkAuto / kSkOff / kSkOn (kPairs = 1 only).
+// *sk tells whether the launch used stream-K.
+template <int kKind, int kPairs, int kWide = 1>
+bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, Params p,
+                 cudaStream_t stream, int sk_mode = kSkOff, bool *sk = nullptr)
+{
+    if (sk) *sk = false;
     const int clusters = pair_clusters<kKind, kPairs, kWide>();
     if (clusters <= 0) return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
@@ -1587,6 +1912,32 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    p.sk_tiles = kPairs == 1 ? stream_k_tiles(tiles, n, p.num_kb, kSkKbUs * kWide, sk_mode) : 0;
+    int dev = -1;
+    SkWorkspace *w = nullptr;
+    if (p.sk_tiles > 0 && !stream_capturing(stream) && cudaGetDevice(&dev) == cudaSuccess)
+        w = sk_workspace(dev);
+    if (w) {
+        std::lock_guard<std::mutex> lock(w->mu);
+        if (sk_ensure(*w, n, stream)) {
+            if (w->recorded && cudaStreamWaitEvent(stream, w->last, 0) != cudaSuccess) {
+                cudaGetLastError();
+                return false;
+            }
+            p.sk_work = w->work;
+            p.sk_flags = w->flags;
+            p.sk_gen = ++w->gen;
+            if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kPairs, kWide>, ma, mb, mc, p) != cudaSuccess) {
+                cudaGetLastError();
+                return false;
+            }
+            w->recorded = cudaEventRecord(w->last, stream) == cudaSuccess;
+            if (!w->recorded) cudaGetLastError();
+            if (sk) *sk = true;
+            return true;
+        }
+    }
+    p.sk_tiles = 0;
     if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kPairs, kWide>, ma, mb, mc, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
@@ -1605,6 +1956,10 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, 
     p.bn = BN;
     p.tma_store = 0;
     p.b3d = 0;
+    p.sk_tiles = 0;
+    p.sk_work = nullptr;
+    p.sk_flags = nullptr;
+    p.sk_gen = 0;
     p.stages = STAGES;
     p.stage_bytes = STAGE_BYTES;
     p.inject_stall = t_inject_limit_ns ? 1 : 0;
@@ -1724,19 +2079,45 @@ UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok, bool x2_ok
     // receives 32 KB per stage, and the shared ring couples the two pairs.
     // It stays reachable through dgemm_tune_next.)
     (void)x2_ok;
-    // 256 x 512 pair tiles carry a quarter fewer operand bytes per flop into
-    // each SM, worth ~3 % per tile (8192 x 8192 x 4096: TF32 1024 vs 994
-    // TFLOP/s), but a wide tile takes twice as long, so it pays only when the
-    // rounds of tiles over the CTA pairs come out no worse: taken when
-    // 2 x 0.97 x rounds(wide) < rounds(256 x 256) (8192 x 8448 x 4096: 14
-    // rounds of pair tiles against 8 of wide ones, TF32 1008 vs 917)
-    const int64_t pairs = sm_count / 2;
-    const int64_t bands = (p.M + PAIR_BM - 1) / PAIR_BM;
-    const int64_t rounds_pair = (bands * ((p.N + BN - 1) / BN) + pairs - 1) / pairs;
-    const int64_t rounds_wide = (bands * ((p.N + 2 * BN - 1) / (2 * BN)) + pairs - 1) / pairs;
-    if (pair_ok && p.M > BM && rounds_wide >= 1 && 2.0 * 0.97 * rounds_wide < rounds_pair)
-        return {kVariantWide, BN, 1};
-    if (tiles256 * 2 > sm_count) return {pair_ok && p.M > BM ? kVariantPair : kVariantSingle, BN, 1};
+    // Problems of more than half a wave of 128 x 256 tiles take a CTA-pair
+    // kernel, with 256 x 256 or 256 x 512 tiles, each with whole tiles dealt
+    // round-robin or with a stream-K tail.  Estimated time, with P pairs,
+    // T tiles and t the time of a 256 x 256 tile (num_kb K blocks):
+    //   round-robin  ceil(T / P) x t_tile
+    //   stream-K     T / P x t_tile + the partials' cost
+    // A 256 x 512 tile takes 2 x f x t: it carries a quarter fewer operand
+    // bytes per flop into each SM, worth f = 0.97 for TF32; the power-bound
+    // 16-bit kinds gain nothing per tile (f = 1).  Stream-K costs ~8 us with
+    // 256 x 256 tiles and, with 256 x 512 tiles (one accumulator, so every
+    // extra unit of work stalls the MMAs for a drain), ~3 + 5 x (bytes per C
+    // element) us.  Fitted to GB300 sweeps (8192 x 8192 x 4096, n^3 for n =
+    // 4096, 12288, 16384, 8192 x 8448 x 4096, FP16 and TF32); ties go to
+    // the earlier of wide / pair round-robin, wide / pair stream-K.
+    if (pair_ok && p.M > BM && tiles256 * 2 > sm_count) {
+        const int64_t pairs = sm_count / 2;
+        const int64_t bands = (p.M + PAIR_BM - 1) / PAIR_BM;
+        const int64_t tp = bands * ((p.N + BN - 1) / BN), tw = bands * ((p.N + 2 * BN - 1) / (2 * BN));
+        const double t = static_cast<double>(p.num_kb) * kSkKbUs;
+        const double f = T::kElem == 4 ? 0.97 : 1.0;
+        const double ovh_w = 3.0 + 5.0 * (T::kElem == 4 ? 4 : 2), ovh_p = 8.0;
+        auto rr = [&](int64_t tiles) { return static_cast<double>((tiles + pairs - 1) / pairs); };
+        auto fr = [&](int64_t tiles) { return static_cast<double>(tiles) / static_cast<double>(pairs); };
+        const bool sk_w = tw > pairs && tw % pairs != 0, sk_p = tp > pairs && tp % pairs != 0;
+        struct Cand {
+            double us;
+            UmmaConfig cfg;
+        } cand[4] = {
+            {rr(tw) * 2.0 * f * t, {kVariantWide, BN, kSkOff}},
+            {rr(tp) * t, {kVariantPair, BN, kSkOff}},
+            {sk_w ? fr(tw) * 2.0 * f * t + ovh_w : 1e30, {kVariantWide, BN, kSkOn}},
+            {sk_p ? fr(tp) * t + ovh_p : 1e30, {kVariantPair, BN, kSkOn}},
+        };
+        int best = 0;
+        for (int i = 1; i < 4; ++i)
+            if (cand[i].us < cand[best].us * 0.995) best = i;
+        return cand[best].cfg;
+    }
+    if (tiles256 * 2 > sm_count) return {kVariantSingle, BN, 1};
     const double kb_mma_us = 0.33 / 256.0;          // per column of bn, one K block
     const double sm_bytes_per_us = 75e3;            // 75 GB/s
     const double hbm_bytes_per_us = 6.0e6;          // 6 TB/s
@@ -1793,9 +2174,9 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorM
 // [0] pair, [1] register / cp.async producer, then per tile width bn
 // (32..256) the single-CTA TMA kernel and split-K S = 2..8.
 template <int kKind>
-const char *variant_name(int variant, int bn = BN, int split = 1)
+const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = false)
 {
-    static std::string names[4 + 9 * 9];
+    static std::string names[6 + 9 * 9];
     static std::once_flag once;
     std::call_once(once, [] {
         using T = Traits<kKind>;
@@ -1806,6 +2187,8 @@ const char *variant_name(int variant, int bn = BN, int split = 1)
         names[0] = base + "_pair_256x256x" + bk + "_tma";
         names[2 + 9 * 9] = base + "_pair_x2_256x512x" + bk + "_tma";
         names[3 + 9 * 9] = base + "_pair_256x512x" + bk + "_tma";
+        names[4 + 9 * 9] = base + "_pair_256x256x" + bk + "_sk_tma";
+        names[5 + 9 * 9] = base + "_pair_256x512x" + bk + "_sk_tma";
         names[1] = base + "_128x256x" + bk + (kKind == kTF32 ? "_cpasync" : "_ldst");
         for (int w = 1; w <= 8; ++w) {
             const std::string tile = "128x" + std::to_string(32 * w) + "x" + bk;
@@ -1814,9 +2197,9 @@ const char *variant_name(int variant, int bn = BN, int split = 1)
                 names[2 + w * 9 + S] = base + "_splitk" + std::to_string(S) + "_" + tile + "_tma";
         }
     });
-    if (variant == kVariantPair) return names[0].c_str();
+    if (variant == kVariantPair) return names[sk ? 4 + 9 * 9 : 0].c_str();
     if (variant == kVariantQuad) return names[2 + 9 * 9].c_str();
-    if (variant == kVariantWide) return names[3 + 9 * 9].c_str();
+    if (variant == kVariantWide) return names[sk ? 5 + 9 * 9 : 3 + 9 * 9].c_str();
     if (variant == kVariantAuto) return names[1].c_str();  // the non-TMA kernel
     const int w = bn / 32, S = variant == kVariantSplit ? split : 1;
     return names[2 + w * 9 + S].c_str();
@@ -1857,19 +2240,22 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
     if (cfg.variant == kVariantPair || cfg.variant == kVariantQuad || cfg.variant == kVariantWide) {
         p.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
         p.b3d = pair3d;
+        bool sk = false;
         if (cfg.variant == kVariantWide) {
             Params w = p;
             w.bn = 2 * BN;  // 256 x 512 pair tiles
             w.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);
             if (w.bn % box_cols<kKind>() != 0) w.tma_store = 0;
-            if (launch_pair<kKind, 1, 2>(ma, *mb_pair, mc, w, stream)) return variant_name<kKind>(kVariantWide);
+            if (launch_pair<kKind, 1, 2>(ma, *mb_pair, mc, w, stream, cfg.split, &sk))
+                return variant_name<kKind>(kVariantWide, BN, 1, sk);
         }
         if (cfg.variant == kVariantQuad) {
             Params q = p;
             q.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);  // 256 x 512 supertiles
             if (launch_pair<kKind, 2>(*ma_x2, *mb_pair, mc, q, stream)) return variant_name<kKind>(kVariantQuad);
         }
-        if (launch_pair<kKind, 1>(ma, *mb_pair, mc, p, stream)) return variant_name<kKind>(kVariantPair);
+        if (launch_pair<kKind, 1>(ma, *mb_pair, mc, p, stream, cfg.variant == kVariantQuad ? kSkAuto : cfg.split, &sk))
+            return variant_name<kKind>(kVariantPair, BN, 1, sk);
         cfg = UmmaConfig{kVariantSingle, BN, 1};
         p = p0;
     }
@@ -1992,8 +2378,10 @@ int umma_tune_next(int variant, int bn, int split)
     if ((variant == kVariantSingle || variant == kVariantSplit) && (bn < 32 || bn > BN || bn % 32 != 0))
         return DGEMM_ERR_INVALID_ARG;
     if (variant == kVariantSplit && (split < 2 || split > 8)) return DGEMM_ERR_INVALID_ARG;
+    const bool paired = variant == kVariantPair || variant == kVariantWide;
+    if (paired && (split < kSkAuto || split > kSkOn)) return DGEMM_ERR_INVALID_ARG;
     const bool sized = variant == kVariantSingle || variant == kVariantSplit;
-    t_tune = UmmaConfig{variant, sized ? bn : BN, variant == kVariantSplit ? split : 1};
+    t_tune = UmmaConfig{variant, sized ? bn : BN, variant == kVariantSplit || paired ? split : 1};
     return DGEMM_OK;
 }
 

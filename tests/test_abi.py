@@ -120,6 +120,9 @@ def test_tune_next_validates_on_host(L):
     assert L.dgemm_tune_next(3, 128, 1) == 1     # split below 2
     assert L.dgemm_tune_next(3, 128, 9) == 1     # split above 8
     assert L.dgemm_tune_next(3, 128, 4) == 0
+    assert L.dgemm_tune_next(5, 256, 3) == 1     # stream-K mode of a pair variant: 0..2
+    assert L.dgemm_tune_next(1, 256, -1) == 1
+    assert L.dgemm_tune_next(1, 256, 2) == 0
     assert L.dgemm_tune_next(0, 0, 0) == 0       # back to automatic
 
 
