@@ -1797,20 +1797,25 @@ int pair_clusters()
 
 // ---- stream-K workspace
 //
-// One per device, allocated on the first stream-K launch and kept: a slot of
-// partial sums per CTA pair (2 halves x 8 warp regions x 32 KB = 512 KB;
-// 38 MB for 76 pairs) and one 64-bit flag per region.  Launches that use it
-// are ordered one after another, on whatever streams they come from, through
-// an event that each records and the next waits for; each launch stamps its
-// flags with a new generation, so flags left by earlier launches (or by an
-// aborted one) never match.  Stream-K is not used while the stream is being
-// captured into a graph (the graph would hold the shared workspace); the
-// round-robin schedule then runs, with bit-identical results.
+// Static device memory of the library (no call allocates): a slot of partial
+// sums per CTA pair (2 halves x 8 warp regions x 32 KB = 512 KB) for up to
+// SK_MAX_PAIRS pairs, 64 MiB, and one 64-bit flag per region, zero from
+// module load.  Launches that use it are ordered one after another, on
+// whatever streams they come from, through an event that each records and
+// the next waits for; each launch stamps its flags with a new generation, so
+// flags left by earlier launches (or by an aborted one) never match.
+// Stream-K is not used while the stream is being captured into a graph (the
+// graph would hold the shared workspace); the round-robin schedule then
+// runs, with bit-identical results.
+constexpr int SK_MAX_PAIRS = 128;
+constexpr int64_t SK_REGIONS = static_cast<int64_t>(SK_MAX_PAIRS) * 2 * SK_WARP_SLOTS;
+__device__ __align__(256) float g_sk_work[SK_REGIONS * SK_REGION_FLOATS];
+__device__ uint64_t g_sk_flags[SK_REGIONS];
+
 struct SkWorkspace {
     std::mutex mu;
     float *work = nullptr;
     uint64_t *flags = nullptr;
-    int64_t slots = 0;
     cudaEvent_t last = nullptr;
     bool recorded = false;
     bool failed = false;
@@ -1824,31 +1829,23 @@ SkWorkspace *sk_workspace(int dev)
     return dev >= 0 && dev < kMaxDevices ? &ws[dev] : nullptr;
 }
 
-// Allocate the device's workspace for `slots` pairs (once; mu held).
-bool sk_ensure(SkWorkspace &w, int64_t slots, cudaStream_t stream)
+// Resolve the current device's workspace for `slots` pairs (mu held).
+bool sk_ensure(SkWorkspace &w, int64_t slots)
 {
-    if (w.work) return w.slots >= slots;
+    if (slots > SK_MAX_PAIRS) return false;
+    if (w.work) return true;
     if (w.failed) return false;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-        slots = std::max<int64_t>(slots, sms / 2);  // every pair count this device can run
-    const size_t regions = static_cast<size_t>(slots) * 2 * SK_WARP_SLOTS;
     void *work = nullptr, *flags = nullptr;
     cudaEvent_t ev = nullptr;
-    if (cudaMalloc(&work, regions * SK_REGION_FLOATS * sizeof(float)) != cudaSuccess ||
-        cudaMalloc(&flags, regions * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMemsetAsync(flags, 0, regions * sizeof(uint64_t), stream) != cudaSuccess ||
+    if (cudaGetSymbolAddress(&work, g_sk_work) != cudaSuccess ||
+        cudaGetSymbolAddress(&flags, g_sk_flags) != cudaSuccess ||
         cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
         cudaGetLastError();
-        if (work) cudaFree(work);
-        if (flags) cudaFree(flags);
         w.failed = true;
         return false;
     }
     w.work = static_cast<float *>(work);
     w.flags = static_cast<uint64_t *>(flags);
-    w.slots = slots;
     w.last = ev;
     return true;
 }
@@ -1919,7 +1916,7 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
         w = sk_workspace(dev);
     if (w) {
         std::lock_guard<std::mutex> lock(w->mu);
-        if (sk_ensure(*w, n, stream)) {
+        if (sk_ensure(*w, n)) {
             if (w->recorded && cudaStreamWaitEvent(stream, w->last, 0) != cudaSuccess) {
                 cudaGetLastError();
                 return false;

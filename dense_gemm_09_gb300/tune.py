@@ -35,10 +35,13 @@ KINDS = {
 
 
 def configs(step: int, sms: int, M: int, N: int):
-    """Every (variant, bn, split) worth timing: the pair kernel, and for each
-    tile width bn the single-CTA kernel and the splits that fit one wave."""
-    out = [(dg.TUNE_AUTO, 256, 1), (dg.TUNE_PAIR, 256, 1), (dg.TUNE_PAIR_X2, 256, 1),
-           (dg.TUNE_PAIR_WIDE, 256, 1)]
+    """Every (variant, bn, split) worth timing: the pair kernels (256 x 256
+    and 256 x 512 tiles, each round-robin and with the stream-K tail; two
+    pairs per cluster), and for each tile width bn the single-CTA kernel and
+    the splits that fit one wave."""
+    out = [(dg.TUNE_AUTO, 256, 1), (dg.TUNE_PAIR, 256, dg.SK_OFF), (dg.TUNE_PAIR, 256, dg.SK_ON),
+           (dg.TUNE_PAIR_X2, 256, 1), (dg.TUNE_PAIR_WIDE, 256, dg.SK_OFF),
+           (dg.TUNE_PAIR_WIDE, 256, dg.SK_ON)]
     tiles_m = (M + 127) // 128
     for bn in range(256, 31, -step):
         out.append((dg.TUNE_SINGLE, bn, 1))

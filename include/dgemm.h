@@ -27,7 +27,19 @@
  *   are left untouched).
  * Memory: no call allocates device memory or synchronises; results are
  *   ready when the stream reaches the call.  The library keeps a per-device
- *   cache of device properties.
+ *   cache of device properties, and two arrays of static device memory
+ *   (allocated with the library's code when it is loaded): the 64 MiB
+ *   scratch of gemm_tf32_noalloc and the 64 MiB stream-K workspace of the
+ *   tensor-core calls.
+ * Stream-K: when a large problem's output tiles do not divide evenly over
+ *   the CTA pairs, the tensor-core calls may cut the first tiles along K
+ *   (one contiguous range of K blocks per pair).  The pair that finishes a
+ *   cut tile starts from the raw FP32 partial sum the previous pair left in
+ *   the workspace, so results are bit-identical to uncut tiles.  Launches
+ *   that use the workspace are ordered one after another across streams
+ *   through an event (the library records it and makes the next such launch
+ *   wait on it); under stream capture the calls do not cut tiles.  Source:
+ *   none on the pages (their kernels deal whole tiles).
  * Special cases (BLAS conventions):
  *   M == 0 or N == 0  -> DGEMM_OK, nothing is launched;
  *   K == 0 or alpha == 0 -> C = beta * C, A and B are never read; with
@@ -277,7 +289,10 @@ int dgemm_test_inject_stall(uint64_t wait_limit_ns);
  *   bn:    tile width for variants 2 and 3: 32..256 in steps of 32; the
  *          NN 16-bit calls need a multiple of 64.  Ignored otherwise.
  *   split: 2..8 for variant 3 (lowered to the number of K blocks when K is
- *          shorter, so that every CTA has work); ignored otherwise.
+ *          shorter, so that every CTA has work); for variants 1 and 5 the
+ *          stream-K mode: 0 automatic, 1 whole tiles only, 2 cut the first
+ *          P + (T mod P) of T tiles whenever they outnumber the P pairs;
+ *          ignored otherwise.
  * Returns DGEMM_ERR_INVALID_ARG (and records nothing) for values outside
  * these ranges, else DGEMM_OK.  A configuration the next call cannot take
  * (operands that only the register-path kernel can load, or a bn that is not
