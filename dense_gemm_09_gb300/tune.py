@@ -11,6 +11,9 @@ sweeps.
 
     python -m dense_gemm_09_gb300.tune --kind f16_tn --shape 127x12288x4096
 
+With --cublas it also times torch.matmul (cuBLAS) on the same operands and
+flush, as a context line; cuBLAS is never part of the library's path.
+
 Operands are seeded uniform[-1, 1) values on the current GPU; the L2 cache
 is flushed before every timed call, and times are means of CUDA-event
 intervals (the event clock ticks in steps of about 2 us, so means resolve
@@ -26,6 +29,7 @@ import torch
 import dense_gemm_09_gb300 as dg
 
 KINDS = {
+    "f32": (torch.float32, False, dg.gemm_f32, 0),  # SIMT: no tile configurations to sweep
     "tf32": (torch.float32, False, dg.gemm_tf32, 32),
     "f16_tn": (torch.float16, True, dg.gemm_f16_tn, 32),
     "f16_nn": (torch.float16, False, dg.gemm_f16_nn, 64),
@@ -35,10 +39,13 @@ KINDS = {
 
 
 def configs(step: int, sms: int, M: int, N: int):
+    if step == 0:
+        return [(dg.TUNE_AUTO, 256, 1)]
     """Every (variant, bn, split) worth timing: the pair kernels (256 x 256
     and 256 x 512 tiles, each round-robin and with the stream-K tail; two
     pairs per cluster), and for each tile width bn the single-CTA kernel and
-    the splits that fit one wave."""
+    the splits that fit one wave (step 0: the FP32 SIMT call, automatic
+    only)."""
     out = [(dg.TUNE_AUTO, 256, 1), (dg.TUNE_PAIR, 256, dg.SK_OFF), (dg.TUNE_PAIR, 256, dg.SK_ON),
            (dg.TUNE_PAIR_X2, 256, 1), (dg.TUNE_PAIR_WIDE, 256, dg.SK_OFF),
            (dg.TUNE_PAIR_WIDE, 256, dg.SK_ON)]
@@ -52,7 +59,16 @@ def configs(step: int, sms: int, M: int, N: int):
     return out
 
 
-def sweep(kind: str, M: int, N: int, K: int, reps: int = 30, warmup: int = 3, seed: int = 0):
+def cublas_call(kind: str, A, B, out):
+    """The same product through torch.matmul (cuBLAS), for context only: FP32
+    with TF32 disabled, TF32 with it enabled, the TN kinds as A @ B^T."""
+    tn = KINDS[kind][1]
+    torch.backends.cuda.matmul.allow_tf32 = kind == "tf32"
+    torch.mm(A, B.t() if tn else B, out=out)
+
+
+def sweep(kind: str, M: int, N: int, K: int, reps: int = 30, warmup: int = 3, seed: int = 0,
+          cublas: bool = False, cublas_only: bool = False, profile_range: bool = False):
     dtype, tn, fn, step = KINDS[kind]
     dev = torch.device("cuda")
     g = torch.Generator().manual_seed(seed)
@@ -64,8 +80,15 @@ def sweep(kind: str, M: int, N: int, K: int, reps: int = 30, warmup: int = 3, se
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ref = None
     rows = []
-    for variant, bn, split in configs(step, sms, M, N):
+    cases = [] if cublas_only else [(v, bn, sp, None) for v, bn, sp in configs(step, sms, M, N)]
+    if cublas or cublas_only:
+        cases.append((None, 0, 0, "cublas (torch.matmul, context only)"))
+    tf32_flag = torch.backends.cuda.matmul.allow_tf32
+    for variant, bn, split, label in cases:
         def call():
+            if label:
+                cublas_call(kind, A, B, C)
+                return
             if variant != dg.TUNE_AUTO:
                 dg.tune_next(variant, bn, split)
             fn(A, B, C, 1.0, 0.0)
@@ -77,11 +100,15 @@ def sweep(kind: str, M: int, N: int, K: int, reps: int = 30, warmup: int = 3, se
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
+            if profile_range:  # only the timed calls, for `ncu --profile-from-start off`
+                torch.cuda.profiler.start()
             call()
+            if profile_range:
+                torch.cuda.profiler.stop()
             e1.record()
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
-        name = dg.last_kernel()
+        name = label or dg.last_kernel()
         out = C.float()
         if ref is None:
             ref = out.clone()
@@ -89,8 +116,9 @@ def sweep(kind: str, M: int, N: int, K: int, reps: int = 30, warmup: int = 3, se
         diff = (out - ref).abs().max().item() / scale
         ms = statistics.mean(times)
         rows.append((ms, name, variant == dg.TUNE_AUTO, diff))
+    torch.backends.cuda.matmul.allow_tf32 = tf32_flag
     assert dg.device_status() == dg.OK
-    auto_name = rows[0][1]
+    auto_name = rows[0][1] if not cublas_only else ""
     best = {}  # one line per kernel actually run (a request the call cannot take runs the automatic one)
     for ms, name, _, diff in rows:
         if name not in best or ms < best[name][0]:
@@ -103,9 +131,16 @@ def main():
     ap.add_argument("--kind", choices=sorted(KINDS), default="f16_tn")
     ap.add_argument("--shape", required=True, help="MxNxK")
     ap.add_argument("--reps", type=int, default=30)
+    ap.add_argument("--cublas", action="store_true",
+                    help="also time torch.matmul (cuBLAS) on the same operands, for context")
+    ap.add_argument("--cublas-only", action="store_true", help="time only the torch.matmul line")
+    ap.add_argument("--profile-range", action="store_true",
+                    help="bracket each timed call with the profiler start/stop API, so that "
+                         "ncu --profile-from-start off captures those launches and nothing else")
     a = ap.parse_args()
     M, N, K = (int(v) for v in a.shape.lower().split("x"))
-    table = sweep(a.kind, M, N, K, reps=a.reps)
+    table = sweep(a.kind, M, N, K, reps=a.reps, cublas=a.cublas, cublas_only=a.cublas_only,
+                  profile_range=a.profile_range)
     flops = 2.0 * M * N * K
     print("%s %dx%dx%d" % (a.kind, M, N, K))
     for ms, name, auto, diff in table:
