@@ -80,6 +80,12 @@ def lib():
         L.gemm_tf32_workspace_bytes.restype = i64
         L.gemm_tf32_noalloc.argtypes = sig
         L.gemm_tf32_noalloc.restype = ci
+        L.dgemm_test_pair_units.argtypes = [i64, i64, i64, i64, i64, vp, i64]
+        L.dgemm_test_pair_units.restype = i64
+        L.dgemm_test_stream_k_tiles.argtypes = [i64, i64, i64, ci, ci]
+        L.dgemm_test_stream_k_tiles.restype = i64
+        L.dgemm_test_choose_config.argtypes = [ci, i64, i64, i64, ci, vp, vp, vp]
+        L.dgemm_test_choose_config.restype = ci
         _lib = L
         return L
 

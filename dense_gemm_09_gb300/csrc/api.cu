@@ -279,6 +279,23 @@ extern "C" int dgemm_tune_next(int variant, int bn, int split)
     return umma_tune_next(variant, bn, split);
 }
 
+extern "C" int64_t dgemm_test_pair_units(int64_t tiles, int64_t pairs, int64_t num_kb, int64_t sk_tiles,
+                                         int64_t pair, int64_t *out, int64_t max_units)
+{
+    return umma_test_pair_units(tiles, pairs, num_kb, sk_tiles, pair, out, max_units);
+}
+
+extern "C" int64_t dgemm_test_stream_k_tiles(int64_t tiles, int64_t pairs, int64_t num_kb, int wide, int mode)
+{
+    return umma_test_stream_k_tiles(tiles, pairs, num_kb, wide, mode);
+}
+
+extern "C" int dgemm_test_choose_config(int kind, int64_t M, int64_t N, int64_t K, int sm_count, int *variant,
+                                        int *bn, int *split)
+{
+    return umma_test_choose(kind, M, N, K, sm_count, variant, bn, split);
+}
+
 extern "C" int dgemm_test_inject_stall(uint64_t wait_limit_ns)
 {
     umma_inject_stall(wait_limit_ns);

@@ -63,4 +63,11 @@ void umma_inject_stall(uint64_t wait_limit_ns);
 // Tuning hook behind dgemm_tune_next.
 int umma_tune_next(int variant, int bn, int split);
 
+// Test hooks behind dgemm_test_pair_units, dgemm_test_stream_k_tiles and
+// dgemm_test_choose_config (host computation only).
+int64_t umma_test_pair_units(int64_t tiles, int64_t pairs, int64_t num_kb, int64_t sk_tiles, int64_t pair,
+                             int64_t *out, int64_t max_units);
+int64_t umma_test_stream_k_tiles(int64_t tiles, int64_t pairs, int64_t num_kb, int wide, int mode);
+int umma_test_choose(int kind, int64_t M, int64_t N, int64_t K, int sm_count, int *variant, int *bn, int *split);
+
 }  // namespace dgemm

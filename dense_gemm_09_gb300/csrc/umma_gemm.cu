@@ -1236,7 +1236,7 @@ struct WorkIter {
     int64_t t_sk, t_sk_first, b, e;  // stream-K: next tile (descending), first tile, K-block range
     int64_t t_dp, dt_dp, tiles;      // round-robin: next tile, stride, tile count
 
-    __device__ __forceinline__ WorkIter(const Params &p, int64_t cluster, int64_t clusters)
+    __host__ __device__ __forceinline__ WorkIter(const Params &p, int64_t cluster, int64_t clusters)
     {
         tiles = p.tiles_m * p.tiles_n;
         if (p.sk_tiles > 0) {
@@ -1255,12 +1255,12 @@ struct WorkIter {
     }
 
     // whether the unit after the current one is the "init" tail
-    __device__ __forceinline__ bool next_is_init(const Params &p) const
+    __host__ __device__ __forceinline__ bool next_is_init(const Params &p) const
     {
         return t_sk == t_sk_first && b > t_sk_first * p.num_kb;
     }
 
-    __device__ __forceinline__ bool next(const Params &p, Unit &u)
+    __host__ __device__ __forceinline__ bool next(const Params &p, Unit &u)
     {
         if (t_sk >= t_sk_first) {
             const int64_t base = t_sk * p.num_kb;
@@ -2379,6 +2379,75 @@ int umma_tune_next(int variant, int bn, int split)
     if (paired && (split < kSkAuto || split > kSkOn)) return DGEMM_ERR_INVALID_ARG;
     const bool sized = variant == kVariantSingle || variant == kVariantSplit;
     t_tune = UmmaConfig{variant, sized ? bn : BN, variant == kVariantSplit || paired ? split : 1};
+    return DGEMM_OK;
+}
+
+// ---- test hooks: the host-compiled schedule and tile choice (no launch)
+
+int64_t umma_test_pair_units(int64_t tiles, int64_t pairs, int64_t num_kb, int64_t sk_tiles, int64_t pair,
+                             int64_t *out, int64_t max_units)
+{
+    if (tiles < 1 || pairs < 1 || num_kb < 1 || pair < 0 || pair >= pairs || sk_tiles < 0 || sk_tiles > tiles ||
+        (sk_tiles > 0 && sk_tiles < pairs) || max_units < 0 || (max_units > 0 && !out))
+        return -1;
+    Params p{};
+    p.tiles_m = tiles;  // a 1-D tile order is all the schedule sees
+    p.tiles_n = 1;
+    p.num_kb = num_kb;
+    p.sk_tiles = sk_tiles;
+    WorkIter it(p, pair, pairs);
+    Unit u;
+    int64_t n = 0;
+    while (it.next(p, u)) {
+        if (n < max_units) {
+            int64_t *o = out + 5 * n;
+            o[0] = u.t;
+            o[1] = u.k0;
+            o[2] = u.k1;
+            o[3] = u.init ? 1 : 0;
+            o[4] = u.publish ? 1 : 0;
+        }
+        ++n;
+    }
+    return n;
+}
+
+int64_t umma_test_stream_k_tiles(int64_t tiles, int64_t pairs, int64_t num_kb, int wide, int mode)
+{
+    if (wide < 1 || wide > 2 || mode < kSkAuto || mode > kSkOn) return -1;
+    return stream_k_tiles(tiles, pairs, num_kb, kSkKbUs * wide, mode);
+}
+
+template <int kKind>
+UmmaConfig test_choose(int64_t M, int64_t N, int64_t K, int sm_count)
+{
+    Params p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.bn = BN;
+    p.tiles_m = (M + BM - 1) / BM;
+    p.tiles_n = (N + BN - 1) / BN;
+    p.num_kb = (K + Traits<kKind>::BK - 1) / Traits<kKind>::BK;
+    return choose_config<kKind>(p, sm_count, true, true);
+}
+
+int umma_test_choose(int kind, int64_t M, int64_t N, int64_t K, int sm_count, int *variant, int *bn, int *split)
+{
+    if (M < 1 || N < 1 || K < 1 || sm_count < 2 || !variant || !bn || !split) return DGEMM_ERR_INVALID_ARG;
+    UmmaConfig c;
+    switch (kind) {
+    case kF16: c = test_choose<kF16>(M, N, K, sm_count); break;
+    case kTF32: c = test_choose<kTF32>(M, N, K, sm_count); break;
+    case kBF16: c = test_choose<kBF16>(M, N, K, sm_count); break;
+    case kF16NN: c = test_choose<kF16NN>(M, N, K, sm_count); break;
+    case kBF16NN: c = test_choose<kBF16NN>(M, N, K, sm_count); break;
+    default: return DGEMM_ERR_INVALID_ARG;
+    }
+    cudaGetLastError();  // the capacity queries of small problems fail without a GPU
+    *variant = c.variant;
+    *bn = c.bn;
+    *split = c.split;
     return DGEMM_OK;
 }
 

@@ -275,6 +275,44 @@ int dgemm_device_status(int clear);
 int dgemm_test_inject_stall(uint64_t wait_limit_ns);
 
 /*
+ * dgemm_test_pair_units -- TEST HOOK, host computation only (no GPU needed).
+ * Runs the CTA-pair kernels' work schedule, compiled for the host, for a 1-D
+ * order of `tiles` tiles of num_kb K blocks on `pairs` pairs, with the first
+ * sk_tiles tiles in the stream-K region (0, or at least `pairs`).  Writes the
+ * units of pair `pair` in the order the pair runs them, 5 int64 each:
+ * tile, first K block, end K block, init (starts from the previous pair's
+ * partial), publish (leaves its partial for the next pair).  Writes at most
+ * max_units units to out (caller-owned) and returns how many there are, or
+ * -1 for arguments outside those ranges.  Source: none on the pages (their
+ * kernels deal whole tiles).
+ */
+int64_t dgemm_test_pair_units(int64_t tiles, int64_t pairs, int64_t num_kb, int64_t sk_tiles, int64_t pair,
+                              int64_t *out, int64_t max_units);
+
+/*
+ * dgemm_test_stream_k_tiles -- TEST HOOK, host only.  The stream-K region the
+ * pair kernels would use for `tiles` tiles of num_kb K blocks on `pairs`
+ * pairs: wide 1 (256 x 256 tiles) or 2 (256 x 512), mode 0 automatic, 1
+ * never, 2 whenever the tiles outnumber the pairs.  Returns 0 (whole tiles),
+ * pairs + tiles mod pairs, or -1 for an invalid wide or mode.
+ */
+int64_t dgemm_test_stream_k_tiles(int64_t tiles, int64_t pairs, int64_t num_kb, int wide, int mode);
+
+/*
+ * dgemm_test_choose_config -- TEST HOOK, host only.  The tile configuration
+ * the tensor-core calls would choose automatically for an M x N x K problem
+ * of `kind` (0 FP16 TN, 1 TF32, 2 BF16 TN, 3 FP16 NN, 4 BF16 NN) on a
+ * device with sm_count SMs, assuming TMA-capable operands.  Writes the
+ * variant (numbering of dgemm_tune_next), tile width and split / stream-K
+ * mode; returns DGEMM_ERR_INVALID_ARG for non-positive sizes, sm_count < 2,
+ * an unknown kind or a NULL output, else DGEMM_OK.  Small problems, whose
+ * choice queries cluster occupancy on the current device, may choose
+ * differently without a GPU.
+ */
+int dgemm_test_choose_config(int kind, int64_t M, int64_t N, int64_t K, int sm_count, int *variant, int *bn,
+                             int *split);
+
+/*
  * dgemm_tune_next -- TUNING HOOK.  Fixes the tile configuration of the next
  * tensor-core call (gemm_tf32, gemm_f16_*, gemm_bf16_*) made by the calling
  * host thread; one call only, after which the automatic choice resumes.
