@@ -14,8 +14,10 @@ GEMM a 512 MiB buffer is written to flush the 129 MB L2 and a 256 MiB buffer
 is read so the lines left behind are clean (both outside the events).
 The e2e number runs the same GEMMs through the public API with the operands
 in pinned host memory: host->device copies of A and B, the call, and the
-device->host copy of C are all inside its timed region; the copies run on
-their own streams so that they overlap the neighbouring paths' GEMMs.
+device->host copy of C are all inside its timed region, every step; the
+copies run on their own streams, and each path has two device buffer sets
+used by alternate steps, so that one step's copies overlap the GEMMs of the
+steps around it.
 
 --impl reference times the CPU oracle (the only other implementation of the
 method here) on a bounded sample of the same workload: full rows of C for
@@ -265,43 +267,46 @@ def run_ours(args):
     value = total_flops / (ms_step * 1e-3) / 1e12
 
     # ---- end to end through the public API, operands in pinned host memory.
-    # Three streams: host->device copies, the GEMMs, device->host copies.  The
-    # copies of one path's operands overlap the previous path's GEMM and the
-    # read-back of its C overlaps the next GEMM; every path owns its device
-    # buffers, and events keep each buffer's writer behind its last reader.
+    # Three streams: host->device copies, the GEMMs, device->host copies.
+    # Every path owns two sets of device buffers, used by alternate steps, so
+    # that a step's operands travel while the previous step computes and its
+    # C is read back while the next step computes; events keep each buffer's
+    # writer behind its last reader.
     e2e = None
     if not args.no_e2e:
         hosts_c = {p: torch.empty((Mx, Nx), dtype=ops[p][4].dtype).pin_memory() for p in paths_run}
-        dev_bufs = {p: (torch.empty_like(ops[p][2]), torch.empty_like(ops[p][3]),
-                        torch.empty_like(ops[p][4])) for p in paths_run}
+        dev_bufs = {p: [(torch.empty_like(ops[p][2]), torch.empty_like(ops[p][3]), torch.empty_like(ops[p][4]))
+                        for _ in range(2)] for p in paths_run}
         h2d = sum(ops[p][0].numel() * ops[p][0].element_size() + ops[p][1].numel() * ops[p][1].element_size()
                   for p in paths_run)
         d2h = sum(hosts_c[p].numel() * hosts_c[p].element_size() for p in paths_run)
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        ev = {p: {k: torch.cuda.Event() for k in ("in", "gemm", "out")} for p in paths_run}
+        ev = {p: [{k: torch.cuda.Event() for k in ("in", "gemm", "out")} for _ in range(2)] for p in paths_run}
 
-        def e2e_step():
+        def e2e_step(i):
+            b = i % 2
             for p in paths_run:
                 Ah, Bh = ops[p][0], ops[p][1]
-                Ad, Bd, _ = dev_bufs[p]
-                s_in.wait_event(ev[p]["gemm"])          # last GEMM on Ad, Bd has finished
+                Ad, Bd, _ = dev_bufs[p][b]
+                s_in.wait_event(ev[p][b]["gemm"])       # last GEMM on this set's Ad, Bd has finished
                 with torch.cuda.stream(s_in):
                     Ad.copy_(Ah, non_blocking=True)
                     Bd.copy_(Bh, non_blocking=True)
-                ev[p]["in"].record(s_in)
+                ev[p][b]["in"].record(s_in)
             for p in paths_run:
-                Ad, Bd, Cd = dev_bufs[p]
-                stream.wait_event(ev[p]["in"])
-                stream.wait_event(ev[p]["out"])         # last read-back of Cd has finished
+                Ad, Bd, Cd = dev_bufs[p][b]
+                stream.wait_event(ev[p][b]["in"])
+                stream.wait_event(ev[p][b]["out"])      # last read-back of this set's Cd has finished
                 fns[p](Ad, Bd, Cd, 1.0, 0.0, stream=stream)
-                ev[p]["gemm"].record(stream)
-                s_out.wait_event(ev[p]["gemm"])
+                ev[p][b]["gemm"].record(stream)
+                s_out.wait_event(ev[p][b]["gemm"])
                 with torch.cuda.stream(s_out):
                     hosts_c[p].copy_(Cd, non_blocking=True)
-                ev[p]["out"].record(s_out)
+                ev[p][b]["out"].record(s_out)
 
         e2e_steps = max(1, min(args.steps, 10))
-        e2e_step()
+        e2e_step(0)
+        e2e_step(1)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -309,20 +314,23 @@ def run_ours(args):
         e0.record(stream)
         s_in.wait_event(e0)
         s_out.wait_event(e0)
-        for _ in range(e2e_steps):
-            e2e_step()
+        for i in range(e2e_steps):
+            e2e_step(i)
         for p in paths_run:
-            stream.wait_event(ev[p]["out"])
+            for b in range(2):
+                stream.wait_event(ev[p][b]["out"])
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+        last = (e2e_steps - 1) % 2
         for p in paths_run:                               # the read-back is the product
-            torch.testing.assert_close(hosts_c[p], dev_bufs[p][2].cpu(), rtol=0, atol=0)
+            torch.testing.assert_close(hosts_c[p], dev_bufs[p][last][2].cpu(), rtol=0, atol=0)
         e2e = {"value": round(total_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
-               "how": "per path: pinned host A, B -> device, the C-ABI call, C -> pinned host; "
-                      "copies on their own streams overlap the neighbouring paths' GEMMs"}
+               "how": "per path and step: pinned host A, B -> device, the C-ABI call, C -> pinned host; "
+                      "copies on their own streams, two device buffer sets used by alternate steps, so "
+                      "a step's copies overlap the neighbouring steps' GEMMs"}
     assert dg.device_status() == dg.OK
 
     peaks = _peaks()
