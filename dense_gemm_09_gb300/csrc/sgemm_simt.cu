@@ -52,7 +52,7 @@ constexpr int BK = 16;
 constexpr int STAGES = 4;
 constexpr int THREADS = 256;
 constexpr int AS_LD = BM + 4;  // padded row of the transposed A slice
-constexpr int kGroupM = 8;     // rasterisation group height, in tiles
+constexpr int kGroupM = 16;    // rasterisation group height, in tiles
 
 struct SimtStage {
     float As[BK][AS_LD];
