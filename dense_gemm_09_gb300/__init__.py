@@ -106,7 +106,7 @@ def test_inject_stall(wait_limit_ns: int) -> None:
 
 
 # Tile configurations for tune_next (see dgemm_tune_next in include/dgemm.h)
-TUNE_AUTO, TUNE_PAIR, TUNE_SINGLE, TUNE_SPLIT, TUNE_PAIR_X2, TUNE_PAIR_WIDE = 0, 1, 2, 3, 4, 5
+TUNE_AUTO, TUNE_PAIR, TUNE_SINGLE, TUNE_SPLIT, TUNE_PAIR_WIDE = 0, 1, 2, 3, 5
 # `split` of the CTA-pair variants (TUNE_PAIR, TUNE_PAIR_WIDE): stream-K tail
 # chosen automatically, never, or whenever the tiles outnumber the pairs
 SK_AUTO, SK_OFF, SK_ON = 0, 1, 2
@@ -114,7 +114,7 @@ SK_AUTO, SK_OFF, SK_ON = 0, 1, 2
 
 def tune_next(variant: int, bn: int = 256, split: int = 1) -> None:
     """Tuning hook: fix the tile configuration of the next tensor-core call
-    on this thread (variant TUNE_PAIR / TUNE_PAIR_X2 / TUNE_PAIR_WIDE /
+    on this thread (variant TUNE_PAIR / TUNE_PAIR_WIDE /
     TUNE_SINGLE / TUNE_SPLIT, tile width bn, split-K factor split; for
     TUNE_PAIR and TUNE_PAIR_WIDE, split is the stream-K mode SK_*)."""
     st = lib().dgemm_tune_next(int(variant), int(bn), int(split))

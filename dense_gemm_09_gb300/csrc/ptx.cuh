@@ -116,20 +116,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
-// tma_load_2d_pair delivered to every CTA of `cta_mask` (same shared-memory
-// offset in each); each destination's transaction bytes complete on the
-// barrier at the offset of bar_cluster in that destination's pair leader
-// (the even CTA of its pair), the CTA whose pair bit bar_cluster selects.
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const void *tmap, uint32_t bar_cluster,
-                                                           int32_t c0, int32_t c1, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
 // 3-D form of tma_load_2d_pair (coordinates innermost first).
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap, uint32_t bar_cluster,
                                                  int32_t c0, int32_t c1, int32_t c2)

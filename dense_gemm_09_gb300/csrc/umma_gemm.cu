@@ -1176,20 +1176,10 @@ constexpr uint32_t pair_idesc()
     return (Traits<kKind>::kIdesc & ~(0x1Fu << 24)) | (static_cast<uint32_t>(PAIR_BM >> 4) << 24);
 }
 
-// Clusters of kPairs CTA pairs (2 * kPairs CTAs; the pair of rank r is r / 2,
-// its leader the even CTA 2 * (r / 2)).  With kPairs = 2 the two pairs take
-// side-by-side output tiles of the same 256 rows -- a 256 x 512 supertile --
-// and share its A band: each CTA loads 64 of its half's 128 rows and
-// multicasts them to the same half of both pairs, so a CTA reads 24 KB per
-// stage from L2 instead of 32 KB.  The stage ring of every CTA is then
-// written by both pairs' producers, so each "empty" barrier counts one
-// commit from each pair's MMA warp.
-template <int kPairs>
-__device__ __forceinline__ void pair_tile(int64_t t, const Params &p, uint32_t rank, int64_t &m0,
-                                          int64_t &n0)
+// Output tile of pair tile t: 256 rows from m0, p.bn columns from n0.
+__device__ __forceinline__ void pair_tile(int64_t t, const Params &p, int64_t &m0, int64_t &n0)
 {
-    tile_coords(t, p, m0, n0, PAIR_BM);  // n0: supertile column x BN
-    n0 = n0 * kPairs + static_cast<int64_t>(rank >> 1) * BN;
+    tile_coords(t, p, m0, n0, PAIR_BM);
 }
 
 // Pair tiles of 256 x (256 * kWide): with kWide = 2 each MMA step is two
@@ -1390,18 +1380,15 @@ __device__ __forceinline__ bool sk_init(const Params &p, uint32_t taddr, int64_t
     return true;
 }
 
-template <int kKind, int kPairs, int kWide>
+template <int kKind, int kWide>
 __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
                                               const Params &p, uint32_t smem_base, PairCtrl *ctrl,
                                               uint32_t rank, WaitCtl *wc)
 {
     using T = Traits<kKind>;
     using S = PairShape<kWide>;
-    constexpr int kCtas = 2 * kPairs;
-    constexpr int kRowsA = 128 / kPairs;  // A rows this CTA loads per stage
-    constexpr uint16_t kHalfMask = kPairs == 1 ? 0x1 : 0x5;  // the even CTA of every pair
-    const int64_t cluster = blockIdx.x / kCtas, clusters = gridDim.x / kCtas;
-    const uint32_t half = rank & 1u, pair = rank >> 1, leader = rank & ~1u;
+    const int64_t cluster = blockIdx.x / 2, clusters = gridDim.x / 2;
+    const uint32_t half = rank & 1u;
     uint32_t stage = 0, phase = 0;
     uint32_t issued = 0, issued_phase = 0;
     bool ok = true;
@@ -1409,23 +1396,18 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
     Unit u;
     while (ok && it.next(p, u)) {
         int64_t m0, n0;
-        pair_tile<kPairs>(u.t, p, rank, m0, n0);
+        pair_tile(u.t, p, m0, n0);
         for (int64_t kb = u.k0; kb < u.k1; ++kb) {
             if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
                 ok = false;
                 break;
             }
             const uint32_t full_local = ptx::smem_addr(&ctrl->full[stage]);
-            const uint32_t full = ptx::mapa(full_local, leader);  // the pair leader's barrier
+            const uint32_t full = ptx::mapa(full_local, 0);  // the pair leader's barrier
             if (half == 0) ptx::mbar_arrive_expect_tx(full_local, 2 * S::kStageBytes);
             const uint32_t sa = smem_base + stage * S::kStageBytes;
             const int32_t kc = static_cast<int32_t>(kb * T::BK);
-            const int32_t ma = static_cast<int32_t>(m0 + half * 128 + pair * kRowsA);
-            if constexpr (kPairs == 1)
-                ptx::tma_load_2d_pair(sa, tmap_a, full, kc, ma);
-            else
-                ptx::tma_load_2d_pair_multicast(sa + pair * kRowsA * ROW_BYTES, tmap_a, full, kc, ma,
-                                                static_cast<uint16_t>(kHalfMask << half));
+            ptx::tma_load_2d_pair(sa, tmap_a, full, kc, static_cast<int32_t>(m0 + half * 128));
 #pragma unroll
             for (int w = 0; w < kWide; ++w) {
                 const uint32_t sb = sa + (1 + w) * PAIR_HALF_BYTES;
@@ -1465,11 +1447,11 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
 // named barrier 1 + stage.  The barrier's OR-reduction carries the abort flag
 // both ways, so each side runs through the same number of hand-offs and
 // neither can be left waiting on the other after a time-out.
-template <int kKind, int kPairs, int kWide>
+template <int kKind, int kWide>
 __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int lane, WaitCtl *wc)
 {
     using S = PairShape<kWide>;
-    const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
+    const int64_t cluster = blockIdx.x / 2, clusters = gridDim.x / 2;
     uint32_t stage = 0, phase = 0;
     bool abort = false;
     WorkIter it(p, cluster, clusters);
@@ -1492,18 +1474,16 @@ __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int
 
 // A pair's MMA warp (warp 1 of the leader; lane 0 issues).  Per stage it
 // takes the hand-off from the waiter, issues the stage's MMAs and commits the
-// stage's release to the "empty" barriers of every CTA of the cluster (with
-// two pairs, both pairs' producers write each CTA's ring); per tile it waits
-// for a free accumulator and commits "tmem_full" to its own pair.
-template <int kKind, int kPairs, int kWide>
+// stage's release to the "empty" barriers of both CTAs; per tile it waits
+// for a free accumulator and commits "tmem_full" to both CTAs.
+template <int kKind, int kWide>
 __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, PairCtrl *ctrl,
                                          uint32_t tmem_base, uint32_t rank, int lane, WaitCtl *wc)
 {
     using T = Traits<kKind>;
     using S = PairShape<kWide>;
-    constexpr uint16_t kAll = static_cast<uint16_t>((1u << (2 * kPairs)) - 1u);
-    const uint16_t kPair = static_cast<uint16_t>(0x3u << rank);
-    const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
+    constexpr uint16_t kBoth = 0x3;  // the two CTAs of the pair
+    const int64_t cluster = blockIdx.x / 2, clusters = gridDim.x / 2;
     uint32_t stage = 0, acc = 0, acc_phase = 0, ready_phase = 0;
     // test hook: wait on a barrier nothing arrives at, so the wait runs out
     bool ok = true;
@@ -1544,13 +1524,13 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
                                                   (kb != u.k0 || k != 0) ? 1u : acc_first);
                         }
                     }
-                    ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), kAll);
+                    ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), kBoth);
                 }
                 __syncwarp();
             }
             if (++stage == S::kStages) stage = 0;
         }
-        if (!abort && lane == 0) ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->tmem_full[acc]), kPair);
+        if (!abort && lane == 0) ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->tmem_full[acc]), kBoth);
         __syncwarp();
         if (++acc == S::kAccs) {
             acc = 0;
@@ -1564,12 +1544,12 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
     __syncwarp();
 }
 
-template <int kKind, int kPairs, int kWide>
+template <int kKind, int kWide>
 __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap *tmap_c,
                                               PairCtrl *ctrl, uint32_t tmem_base, uint32_t epi_smem,
                                               uint32_t rank, int warp, int lane, WaitCtl *wc)
 {
-    const int64_t cluster = blockIdx.x / (2 * kPairs), clusters = gridDim.x / (2 * kPairs);
+    const int64_t cluster = blockIdx.x / 2, clusters = gridDim.x / 2;
     const uint32_t quarter = static_cast<uint32_t>(warp & 3);
     const uint32_t leader = rank & ~1u;
     // kWide = 2: warps 2-5 drain columns 0-255, warps 7-10 columns 256-511
@@ -1583,7 +1563,7 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap
     Unit u;
     while (it.next(p, u)) {
         int64_t m0, n0;
-        pair_tile<kPairs>(u.t, p, rank, m0, n0);
+        pair_tile(u.t, p, m0, n0);
         const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * PairShape<kWide>::kAccCols +
                                colhalf * BN;
         // Stream-K "init": load the previous pair's partial into the unit's
@@ -1630,7 +1610,7 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap
     if (lane == 0) ptx::bulk_wait<0>();  // stores done before the CTA leaves
 }
 
-template <int kKind, int kPairs, int kWide>
+template <int kKind, int kWide>
 __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     umma_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
@@ -1647,7 +1627,7 @@ __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < PAIR_STAGES; ++s) {
             ptx::mbar_init(ptx::smem_addr(&ctrl->full[s]), 1);
-            ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), kPairs);
+            ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_full[a]), 1);
@@ -1677,13 +1657,13 @@ __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     const uint32_t smem_base = ptx::smem_addr(smem);
 
     if (warp == 0) {
-        if (lane == 0) pair_producer<kKind, kPairs, kWide>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
+        if (lane == 0) pair_producer<kKind, kWide>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
     } else if (warp == PAIR_MMA_WARP) {
-        if (leader) pair_mma<kKind, kPairs, kWide>(p, smem_base, ctrl, tmem_base, rank, lane, wc);
+        if (leader) pair_mma<kKind, kWide>(p, smem_base, ctrl, tmem_base, rank, lane, wc);
     } else if (warp == PAIR_WAITER_WARP) {
-        if (leader) pair_waiter<kKind, kPairs, kWide>(p, ctrl, lane, wc);
+        if (leader) pair_waiter<kKind, kWide>(p, ctrl, lane, wc);
     } else {
-        pair_epilogue<kKind, kPairs, kWide>(p, &tmap_c, ctrl, tmem_base, smem_base + PAIR_STAGES * PAIR_STAGE_BYTES,
+        pair_epilogue<kKind, kWide>(p, &tmap_c, ctrl, tmem_base, smem_base + PAIR_STAGES * PAIR_STAGE_BYTES,
                                      rank, warp, lane, wc);
     }
 
@@ -1760,9 +1740,9 @@ bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
     return true;
 }
 
-// Co-resident clusters of the pair kernel (clusters of 2 * kPairs CTAs) on the
+// Co-resident clusters of the pair kernel (clusters of 2 CTAs) on the
 // current device (0 if the kernel cannot run), cached per device and kind.
-template <int kKind, int kPairs, int kWide = 1>
+template <int kKind, int kWide = 1>
 int pair_clusters()
 {
     constexpr int kMaxDevices = 64;
@@ -1772,22 +1752,22 @@ int pair_clusters()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     std::call_once(once[dev], [dev] {
         int n = 0;
-        if (cudaFuncSetAttribute(umma_pair_kernel<kKind, kPairs, kWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(umma_pair_kernel<kKind, kWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PAIR_SMEM_BYTES) == cudaSuccess) {
             int sms = 0;
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2 * kPairs;
+            attr[0].val.clusterDim.x = 2;
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % (2 * kPairs)));
+            cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % 2));
             cfg.blockDim = dim3(pair_threads<kWide>());
             cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, umma_pair_kernel<kKind, kPairs, kWide>, &cfg) != cudaSuccess) n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, umma_pair_kernel<kKind, kWide>, &cfg) != cudaSuccess) n = 0;
         }
         cudaGetLastError();  // a failed query leaves no sticky error behind
         cached[dev] = n;
@@ -1885,31 +1865,31 @@ int64_t stream_k_tiles(int64_t tiles, int64_t pairs, int64_t num_kb, double kb_u
     return saved_us > kSkMinSavedUs ? pairs + r : 0;
 }
 
-// p.tiles_m / p.tiles_n count 256-row bands and supertile columns (256 * kPairs
-// columns each).  sk_mode: kSkAuto / kSkOff / kSkOn (kPairs = 1 only).
+// p.tiles_m / p.tiles_n count 256-row bands and tile columns (p.bn columns
+// each).  sk_mode: kSkAuto / kSkOff / kSkOn.
 // *sk tells whether the launch used stream-K.
-template <int kKind, int kPairs, int kWide = 1>
+template <int kKind, int kWide = 1>
 bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, Params p,
                  cudaStream_t stream, int sk_mode = kSkOff, bool *sk = nullptr)
 {
     if (sk) *sk = false;
-    const int clusters = pair_clusters<kKind, kPairs, kWide>();
+    const int clusters = pair_clusters<kKind, kWide>();
     if (clusters <= 0) return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
     const int64_t n = tiles < clusters ? tiles : clusters;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2 * kPairs;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * kPairs * n));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
     cfg.blockDim = dim3(pair_threads<kWide>());
     cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    p.sk_tiles = kPairs == 1 ? stream_k_tiles(tiles, n, p.num_kb, kSkKbUs * kWide, sk_mode) : 0;
+    p.sk_tiles = stream_k_tiles(tiles, n, p.num_kb, kSkKbUs * kWide, sk_mode);
     int dev = -1;
     SkWorkspace *w = nullptr;
     if (p.sk_tiles > 0 && !stream_capturing(stream) && cudaGetDevice(&dev) == cudaSuccess)
@@ -1924,7 +1904,7 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
             p.sk_work = w->work;
             p.sk_flags = w->flags;
             p.sk_gen = ++w->gen;
-            if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kPairs, kWide>, ma, mb, mc, p) != cudaSuccess) {
+            if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide>, ma, mb, mc, p) != cudaSuccess) {
                 cudaGetLastError();
                 return false;
             }
@@ -1935,7 +1915,7 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
         }
     }
     p.sk_tiles = 0;
-    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kPairs, kWide>, ma, mb, mc, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide>, ma, mb, mc, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -2029,7 +2009,8 @@ int cluster_capacity(int size)
 // Tile configuration of one call: the CTA-pair kernel (256 x 256 tiles), the
 // persistent single-CTA kernel (128 x bn tiles) or split-K over S CTAs of a
 // cluster (128 x bn tiles).
-enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3, kVariantQuad = 4, kVariantWide = 5 };
+// (4 is unused: it once named a two-pair cluster variant, since removed.)
+enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3, kVariantWide = 5 };
 struct UmmaConfig {
     int variant;
     int bn;
@@ -2064,18 +2045,13 @@ constexpr int bn_step()
 // ~0.33 us, a CTA streams ~75 GB/s, HBM ~6 TB/s; a split costs ~1 us plus
 // ~0.5 us per extra rank plus ~0.9 us per 64 KB of partials moved.
 template <int kKind>
-UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok, bool x2_ok)
+UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok)
 {
     using T = Traits<kKind>;
     const int64_t tiles256 = p.tiles_m * ((p.N + BN - 1) / BN);
     // more than half a wave of 128 x 256 tiles: the pair halves each CTA's
     // operand traffic (2048^3: FP16 21.3 us pair, 22.0 us single; TF32 31.4
     // and 34.6 us)
-    // (two pairs per cluster sharing A -- x2_ok -- measured slower at 8192 x
-    // 8192 x 4096: TF32 901 vs 994 TFLOP/s, FP16 1755 vs 1778; each SM still
-    // receives 32 KB per stage, and the shared ring couples the two pairs.
-    // It stays reachable through dgemm_tune_next.)
-    (void)x2_ok;
     // Problems of more than half a wave of 128 x 256 tiles take a CTA-pair
     // kernel, with 256 x 256 or 256 x 512 tiles, each with whole tiles dealt
     // round-robin or with a stream-K tail.  Estimated time, with P pairs,
@@ -2173,7 +2149,7 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorM
 template <int kKind>
 const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = false)
 {
-    static std::string names[6 + 9 * 9];
+    static std::string names[6 + 9 * 9];  // [2 + 9 * 9] unused
     static std::once_flag once;
     std::call_once(once, [] {
         using T = Traits<kKind>;
@@ -2182,7 +2158,6 @@ const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = fals
         const std::string bk = std::to_string(T::BK);
         const std::string base = std::string("umma_") + kind;
         names[0] = base + "_pair_256x256x" + bk + "_tma";
-        names[2 + 9 * 9] = base + "_pair_x2_256x512x" + bk + "_tma";
         names[3 + 9 * 9] = base + "_pair_256x512x" + bk + "_tma";
         names[4 + 9 * 9] = base + "_pair_256x256x" + bk + "_sk_tma";
         names[5 + 9 * 9] = base + "_pair_256x512x" + bk + "_sk_tma";
@@ -2195,7 +2170,6 @@ const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = fals
         }
     });
     if (variant == kVariantPair) return names[sk ? 4 + 9 * 9 : 0].c_str();
-    if (variant == kVariantQuad) return names[2 + 9 * 9].c_str();
     if (variant == kVariantWide) return names[sk ? 5 + 9 * 9 : 3 + 9 * 9].c_str();
     if (variant == kVariantAuto) return names[1].c_str();  // the non-TMA kernel
     const int w = bn / 32, S = variant == kVariantSplit ? split : 1;
@@ -2217,24 +2191,21 @@ void set_ring(Params &p, bool split)
 // pair kernel (null if B cannot be described); make_b(bn, map) builds B's map
 // for 128 x bn tiles.
 template <int kKind, typename MakeB>
-const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *ma_x2,
-                         const CUtensorMap *mb_pair, int pair3d, MakeB make_b, const CUtensorMap &mc,
+const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *mb_pair, int pair3d, MakeB make_b, const CUtensorMap &mc,
                          cudaStream_t stream, const DeviceInfo &dev)
 {
     UmmaConfig cfg = t_tune;
     t_tune = UmmaConfig{kVariantAuto, BN, 1};
-    if (((cfg.variant == kVariantPair || cfg.variant == kVariantQuad || cfg.variant == kVariantWide) && !mb_pair) ||
-        cfg.bn % bn_step<kKind>() != 0)
+    if (((cfg.variant == kVariantPair || cfg.variant == kVariantWide) && !mb_pair) || cfg.bn % bn_step<kKind>() != 0)
         cfg.variant = kVariantAuto;
-    if (cfg.variant == kVariantQuad && !ma_x2) cfg.variant = kVariantPair;
     // every rank of a split needs at least one K block
     if (cfg.variant == kVariantSplit && cfg.split > p0.num_kb)
         cfg = p0.num_kb >= 2 ? UmmaConfig{kVariantSplit, cfg.bn, static_cast<int>(p0.num_kb)}
                              : UmmaConfig{kVariantSingle, cfg.bn, 1};
     if (cfg.variant == kVariantAuto)
-        cfg = choose_config<kKind>(p0, dev.sm_count, mb_pair != nullptr, ma_x2 != nullptr);
+        cfg = choose_config<kKind>(p0, dev.sm_count, mb_pair != nullptr);
     Params p = p0;
-    if (cfg.variant == kVariantPair || cfg.variant == kVariantQuad || cfg.variant == kVariantWide) {
+    if (cfg.variant == kVariantPair || cfg.variant == kVariantWide) {
         p.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
         p.b3d = pair3d;
         bool sk = false;
@@ -2243,15 +2214,10 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
             w.bn = 2 * BN;  // 256 x 512 pair tiles
             w.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);
             if (w.bn % box_cols<kKind>() != 0) w.tma_store = 0;
-            if (launch_pair<kKind, 1, 2>(ma, *mb_pair, mc, w, stream, cfg.split, &sk))
+            if (launch_pair<kKind, 2>(ma, *mb_pair, mc, w, stream, cfg.split, &sk))
                 return variant_name<kKind>(kVariantWide, BN, 1, sk);
         }
-        if (cfg.variant == kVariantQuad) {
-            Params q = p;
-            q.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);  // 256 x 512 supertiles
-            if (launch_pair<kKind, 2>(*ma_x2, *mb_pair, mc, q, stream)) return variant_name<kKind>(kVariantQuad);
-        }
-        if (launch_pair<kKind, 1>(ma, *mb_pair, mc, p, stream, cfg.variant == kVariantQuad ? kSkAuto : cfg.split, &sk))
+        if (launch_pair<kKind, 1>(ma, *mb_pair, mc, p, stream, cfg.split, &sk))
             return variant_name<kKind>(kVariantPair, BN, 1, sk);
         cfg = UmmaConfig{kVariantSingle, BN, 1};
         p = p0;
@@ -2335,11 +2301,7 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
         int probe3d = 0, pair3d = 0;
         if (make_b(BN, &probe, &probe3d)) {
             const bool ok_pair = make_b(128, &mbp, &pair3d);
-            // two pairs per cluster: each CTA loads 64 of its half's A rows
-            CUtensorMap ma_x2{};
-            const bool ok_x2 = make_map(&ma_x2, dt, A, K, M, lda * es, T::BK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-            return dispatch_tma<kKind>(p, ma, ok_x2 ? &ma_x2 : nullptr, ok_pair ? &mbp : nullptr, pair3d, make_b,
-                                       mc, stream, dev);
+            return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, pair3d, make_b, mc, stream, dev);
         }
     }
     t_tune = UmmaConfig{kVariantAuto, BN, 1};
@@ -2371,7 +2333,7 @@ const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, 
 
 int umma_tune_next(int variant, int bn, int split)
 {
-    if (variant < kVariantAuto || variant > kVariantWide) return DGEMM_ERR_INVALID_ARG;
+    if (variant < kVariantAuto || variant > kVariantWide || variant == 4) return DGEMM_ERR_INVALID_ARG;
     if ((variant == kVariantSingle || variant == kVariantSplit) && (bn < 32 || bn > BN || bn % 32 != 0))
         return DGEMM_ERR_INVALID_ARG;
     if (variant == kVariantSplit && (split < 2 || split > 8)) return DGEMM_ERR_INVALID_ARG;
@@ -2429,7 +2391,7 @@ UmmaConfig test_choose(int64_t M, int64_t N, int64_t K, int sm_count)
     p.tiles_m = (M + BM - 1) / BM;
     p.tiles_n = (N + BN - 1) / BN;
     p.num_kb = (K + Traits<kKind>::BK - 1) / Traits<kKind>::BK;
-    return choose_config<kKind>(p, sm_count, true, true);
+    return choose_config<kKind>(p, sm_count, true);
 }
 
 int umma_test_choose(int kind, int64_t M, int64_t N, int64_t K, int sm_count, int *variant, int *bn, int *split)

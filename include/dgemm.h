@@ -320,8 +320,7 @@ int dgemm_test_choose_config(int kind, int64_t M, int64_t N, int64_t K, int sm_c
  *           1: CTA pair, 256 x 256 output tiles;
  *           2: one CTA per 128 x bn tile, persistent grid;
  *           3: split-K, `split` CTAs of a cluster per 128 x bn tile;
- *           4: two CTA pairs per cluster on a 256 x 512 supertile, the
- *              pairs sharing each A tile through TMA multicast;
+ *           4: not a variant (rejected with DGEMM_ERR_INVALID_ARG);
  *           5: CTA pair, 256 x 512 output tiles (one 512-column
  *              accumulator per CTA).
  *   bn:    tile width for variants 2 and 3: 32..256 in steps of 32; the

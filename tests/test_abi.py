@@ -115,6 +115,7 @@ def test_tune_next_validates_on_host(L):
     # out-of-range requests are refused and record nothing (no device needed)
     assert L.dgemm_tune_next(-1, 256, 1) == 1
     assert L.dgemm_tune_next(6, 256, 1) == 1
+    assert L.dgemm_tune_next(4, 256, 1) == 1     # 4 names no variant
     assert L.dgemm_tune_next(2, 48, 1) == 1      # bn not a multiple of 32
     assert L.dgemm_tune_next(2, 288, 1) == 1     # bn above 256
     assert L.dgemm_tune_next(3, 128, 1) == 1     # split below 2

@@ -4,8 +4,9 @@ Each case draws a path, a shape (log-uniform sizes, so tiny, ragged and
 multi-tile problems all appear), row-pitch padding and base offsets (which
 decide between the TMA, cp.async, register-path and scalar kernels), alpha
 and beta (beta = 0 with a NaN-filled C), and a tile configuration forced
-through the tuning hook (the automatic choice, the CTA pair, the wide and
-two-pair variants, a single-CTA width, split-K).  The case list is fixed by
+through the tuning hook (the automatic choice, the CTA pair with whole tiles
+or with the stream-K tail forced on, the wide pair, a single-CTA width,
+split-K).  The case list is fixed by
 its seed, so a failure reproduces.
 """
 import math
@@ -36,7 +37,7 @@ def _cases(n=240, seed=20261202):
             bn = int(rng.choice([64, 128, 192, 256]))
             split = int(rng.integers(2, 5))
             tune = {0: (0, 256, 1), 1: (1, 256, 1), 2: (2, bn, 1), 3: (3, bn, split),
-                    4: (4, 256, 1), 5: (5, 256, 1)}[kind]
+                    4: (1, 256, 2), 5: (5, 256, 1)}[kind]
         out.append((path, (M, N, K), pad, offset, alpha, beta, tune))
     return out
 

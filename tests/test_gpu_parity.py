@@ -293,32 +293,6 @@ def test_pair_kernel_n_major_b(path, N):
 
 
 @pytest.mark.parametrize("path", parity.TC_PATHS)
-@pytest.mark.parametrize("shape", [(300, 520, 264), (520, 1000, 200), (1000, 768, 520), (257, 1536, 64)])
-def test_pair_x2_kernel(path, shape):
-    import dense_gemm_09_gb300 as dg
-    # two CTA pairs per cluster on 256 x 512 supertiles, sharing A through
-    # TMA multicast; N not a multiple of 512 leaves the second pair's tile
-    # partly (1000, 520) or wholly (300 x 520: 8 columns) outside C
-    M, N, K = shape
-    A, B, C = parity.host_operands(path, M, N, K, seed=M + N)
-    dg.tune_next(dg.TUNE_PAIR_X2)
-    got, _, _ = parity.run(path, A, B, C, 1.25, 0.5)
-    assert "_pair_x2_" in dg.last_kernel(), dg.last_kernel()
-    assert parity.worst_ratio(path, got, A, B, C, 1.25, 0.5) <= 1.0
-
-
-@pytest.mark.parametrize("path", ["tf32", "f16_tn"])
-def test_pair_x2_integers_bit_exact(path):
-    import dense_gemm_09_gb300 as dg
-    A, B, C = parity.host_operands(path, 1024, 2048, 512, seed=5, dist="int")
-    dg.tune_next(dg.TUNE_PAIR_X2)
-    got, _, _ = parity.run(path, A, B, C, 1.0, 1.0)
-    assert "_pair_x2_" in dg.last_kernel()
-    ref, _ = parity.reference(path, A, B, C, 1.0, 1.0)
-    assert np.array_equal(got.double().numpy(), ref)
-
-
-@pytest.mark.parametrize("path", parity.TC_PATHS)
 @pytest.mark.parametrize("shape", [(300, 520, 264), (520, 1000, 200), (1000, 768, 520), (257, 1536, 64),
                                    (129, 300, 40)])
 def test_pair_wide_kernel(path, shape):
