@@ -35,19 +35,18 @@ constexpr int kMaxDevices = 64;
 
 // The device address of g_noalloc_scratch on the current device, looked up
 // on the first call made with that device current (nullptr if the lookup
-// failed).
+// failed).  A failed lookup leaves its error in the runtime's error state for
+// the caller to read with cudaPeekAtLastError / cudaGetLastError; nothing
+// here clears that state, so no error the caller had pending is swallowed.
 void *scratch_address()
 {
     static void *addr[kMaxDevices];
-    static bool ok[kMaxDevices];
     static std::once_flag once[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::call_once(once[dev], [dev] {
         void *p = nullptr;
-        ok[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess && p != nullptr;
-        addr[dev] = ok[dev] ? p : nullptr;
-        if (!ok[dev]) cudaGetLastError();  // leave no error behind for the caller's next call
+        addr[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess ? p : nullptr;
     });
     return addr[dev];
 }
