@@ -166,8 +166,8 @@ def _traffic_for(kernel_file: str, kernel_key: str, shape):
     return e.get("bytes_per_launch") if e.get("source_sha256") == sha else None
 
 
-def _config(paths_run, shape, world, l2=None):
-    """The workload description both arms print."""
+def _config(paths_run, shape, world):
+    """The workload description; both arms print the same one."""
     Mx, Nx, Kx = shape
     default_run = tuple(paths_run) == PATHS and (Mx, Nx, Kx) == (M, N, K)
     return {"workload": ("gemm_f32_tf32_f16tn_8192x8192x4096" if default_run else
@@ -175,8 +175,10 @@ def _config(paths_run, shape, world, l2=None):
             "M": Mx, "N": Nx, "K": Kx,
             "alpha": 1.0, "beta": 0.0, "layout": "row-major NN (f32, tf32); TN (f16)",
             "step": " + ".join("one " + p for p in paths_run),
-            "l2": l2 or "flushed before every GEMM (512 MiB write + 256 MiB read, outside the timed events)",
             "parallelism": "replicas x%d" % world}
+
+
+L2_NOTE = "flushed before every GEMM (512 MiB write + 256 MiB read, outside the timed events)"
 
 
 def run_ours(args):
@@ -283,7 +285,10 @@ def run_ours(args):
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         ev = {p: [{k: torch.cuda.Event() for k in ("in", "gemm", "out")} for _ in range(2)] for p in paths_run}
 
-        def e2e_step(i):
+        gemm_ev = [{p: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for p in paths_run} for _ in range(max(1, min(args.steps, 10)))]
+
+        def e2e_step(i, timed=False):
             b = i % 2
             for p in paths_run:
                 Ah, Bh = ops[p][0], ops[p][1]
@@ -297,7 +302,11 @@ def run_ours(args):
                 Ad, Bd, Cd = dev_bufs[p][b]
                 stream.wait_event(ev[p][b]["in"])
                 stream.wait_event(ev[p][b]["out"])      # last read-back of this set's Cd has finished
+                if timed:
+                    gemm_ev[i][p][0].record(stream)
                 fns[p](Ad, Bd, Cd, 1.0, 0.0, stream=stream)
+                if timed:
+                    gemm_ev[i][p][1].record(stream)
                 ev[p][b]["gemm"].record(stream)
                 s_out.wait_event(ev[p][b]["gemm"])
                 with torch.cuda.stream(s_out):
@@ -315,19 +324,27 @@ def run_ours(args):
         s_in.wait_event(e0)
         s_out.wait_event(e0)
         for i in range(e2e_steps):
-            e2e_step(i)
+            e2e_step(i, timed=True)
         for p in paths_run:
             for b in range(2):
                 stream.wait_event(ev[p][b]["out"])
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+        # the GEMMs' own time inside the e2e leg (no L2 flush there, copies
+        # running beside them), and what the pinned copies alone can move
+        gemm_ms = sum(gemm_ev[i][p][0].elapsed_time(gemm_ev[i][p][1])
+                      for i in range(e2e_steps) for p in paths_run) / e2e_steps
+        bw = _pinned_copy_gbs(torch, dev)
         last = (e2e_steps - 1) % 2
         for p in paths_run:                               # the read-back is the product
             torch.testing.assert_close(hosts_c[p], dev_bufs[p][last][2].cpu(), rtol=0, atol=0)
         e2e = {"value": round(total_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+               "gemm_ms_per_step": round(gemm_ms, 4),
+               "pinned_copy_gbs": bw,
+               "copy_bound_ms_per_step": round(max(h2d / bw["h2d_with_d2h"], d2h / bw["d2h_with_h2d"]) / 1e6, 4),
                "how": "per path and step: pinned host A, B -> device, the C-ABI call, C -> pinned host; "
                       "copies on their own streams, two device buffer sets used by alternate steps, so "
                       "a step's copies overlap the neighbouring steps' GEMMs"}
@@ -370,6 +387,7 @@ def run_ours(args):
         else "+".join(paths_run),
         "data": "synthetic (seeded uniform[-1,1) f32; N(0,1)/sqrt(K) f16)",
         "config": _config(paths_run, (Mx, Nx, Kx), world),
+        "l2": L2_NOTE,
         "paths": paths,
         "roofline": roofline,
         "clocks": clocks,
@@ -382,6 +400,41 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def _pinned_copy_gbs(torch, dev, nbytes=256 * 1024 * 1024, reps=5):
+    """GB/s of pinned host <-> device copies of nbytes: each direction alone,
+    and both at once on two streams (the e2e leg's situation)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s_a, s_b = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(s, fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(reps):
+                fn()
+            e1.record(s)
+        return e0, e1
+
+    out = {}
+    for name, s, fn in (("h2d", s_a, lambda: d_in.copy_(h_in, non_blocking=True)),
+                        ("d2h", s_b, lambda: h_out.copy_(d_out, non_blocking=True))):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = timed(s, fn)
+        torch.cuda.synchronize()
+        out[name] = round(reps * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    torch.cuda.synchronize()
+    a = timed(s_a, lambda: d_in.copy_(h_in, non_blocking=True))
+    b = timed(s_b, lambda: h_out.copy_(d_out, non_blocking=True))
+    torch.cuda.synchronize()
+    out["h2d_with_d2h"] = round(reps * nbytes / (a[0].elapsed_time(a[1]) * 1e-3) / 1e9, 1)
+    out["d2h_with_h2d"] = round(reps * nbytes / (b[0].elapsed_time(b[1]) * 1e-3) / 1e9, 1)
+    return out
 
 
 _ORACLE_OPERANDS = {}
@@ -430,10 +483,14 @@ def _oracle_rows_sample(budget_s: float, nthreads: int = 0):
 
 
 def cpu_baseline(budget_s: float = 15.0):
+    """The oracle on all host cores (the reported value) and on one core."""
     tflops, threads, rows, secs = _oracle_rows_sample(budget_s)
+    t1, _, rows1, secs1 = _oracle_rows_sample(max(budget_s / 3.0, 1.5), nthreads=1)
     return {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": "%d full rows of C (x N=8192, K=4096) across the three paths in %.1f s; "
-                      "operand widening to double not timed" % (rows, secs)}
+                      "operand widening to double not timed" % (rows, secs),
+            "single_core": {"value": round(t1, 6), "unit": "TFLOP/s", "cores": 1,
+                            "sample": "%d full rows of C across the three paths in %.1f s" % (rows1, secs1)}}
 
 
 def run_reference(args):
@@ -460,8 +517,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 accumulation over f32 / tf32 / f16 operand values",
         "data": "synthetic (seeded uniform[-1,1) f32; N(0,1)/sqrt(K) f16)",
-        "config": _config(PATHS, (M, N, K), world,
-                          l2="not applicable: the oracle runs on the host cores"),
+        "config": _config(PATHS, (M, N, K), world),
+        "l2": "not applicable: the oracle runs on the host cores",
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
                          "kind": "oracle",
                          "sample": "%d full rows of C over %d steps (%.1f s per step budget)"
