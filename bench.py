@@ -362,7 +362,9 @@ def run_ours(args):
     dominant = max(paths_run, key=lambda p: paths[p]["ms"])
     dom = paths[dominant]
     simt = dominant in ("f32_simt", "f32_ws")
-    kfile = "sgemm_simt.cu" if simt else "umma_gemm.cu"
+    # the source file whose hash must match the traffic record
+    kfile = ("sgemm_tma.cu" if dom["kernel"].startswith("sgemm_simt_tma") else
+             "sgemm_simt.cu" if simt else "umma_gemm.cu")
     roofline = {"kernel": dom["kernel"],
                 "bound": "alu" if simt else "tensor",
                 "achieved": dom["tflops"], "peak": dom["peak_tflops"], "unit": "TFLOP/s",

@@ -27,11 +27,13 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdgemm.so")
+LIB_CHECKED_PATH = os.path.join(_PKG, "libdgemm_checked.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_BOUNDS = 0, 1, 2, 3, 4, 5
 
 _lock = threading.Lock()
 _lib = None
+_lib_checked = None
 
 
 class DgemmError(RuntimeError):
@@ -41,53 +43,71 @@ class DgemmError(RuntimeError):
 
 
 def build(force: bool = False) -> str:
-    """Compile libdgemm.so (nvcc, sm_103a) in-tree."""
+    """Compile libdgemm.so and the checked build libdgemm_checked.so (nvcc,
+    sm_103a) in-tree; returns the path of libdgemm.so."""
     from . import _build
-    return _build.build(force=force)
+    return _build.build_all(force=force)[0]
 
 
 def lib():
     """The loaded C library, with its signatures declared."""
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError("libdgemm.so is not built (%s); run dense_gemm_09_gb300.build()" % LIB_PATH)
-        L = ctypes.CDLL(LIB_PATH)
-        i64, f32, vp, ci = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
-        sig = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
-        for name in ("gemm_f32", "gemm_tf32", "gemm_f16_tn", "gemm_f16_nn", "gemm_bf16_tn",
-                     "gemm_bf16_nn"):
-            fn = getattr(L, name)
-            fn.argtypes = sig
-            fn.restype = ci
-        L.dgemm_status_string.argtypes = [ci]
-        L.dgemm_status_string.restype = ctypes.c_char_p
-        L.dgemm_device_status.argtypes = [ci]
-        L.dgemm_device_status.restype = ci
-        L.dgemm_test_inject_stall.argtypes = [ctypes.c_uint64]
-        L.dgemm_test_inject_stall.restype = ci
-        L.dgemm_last_kernel.argtypes = []
-        L.dgemm_last_kernel.restype = ctypes.c_char_p
-        L.dgemm_tune_next.argtypes = [ci, ci, ci]
-        L.dgemm_tune_next.restype = ci
-        L.gemm_tf32_ws.argtypes = sig[:11] + [vp, i64, vp]
-        L.gemm_tf32_ws.restype = ci
-        L.gemm_f32_ws.argtypes = sig[:11] + [vp, i64, vp]
-        L.gemm_f32_ws.restype = ci
-        L.gemm_tf32_workspace_bytes.argtypes = [i64, i64, i64, vp, i64, vp, i64]
-        L.gemm_tf32_workspace_bytes.restype = i64
-        L.gemm_tf32_noalloc.argtypes = sig
-        L.gemm_tf32_noalloc.restype = ci
-        L.dgemm_test_pair_units.argtypes = [i64, i64, i64, i64, i64, vp, i64]
-        L.dgemm_test_pair_units.restype = i64
-        L.dgemm_test_stream_k_tiles.argtypes = [i64, i64, i64, ci, ci]
-        L.dgemm_test_stream_k_tiles.restype = i64
-        L.dgemm_test_choose_config.argtypes = [ci, i64, i64, i64, ci, vp, vp, vp]
-        L.dgemm_test_choose_config.restype = ci
-        _lib = L
-        return L
+        if _lib is None:
+            _lib = _load(LIB_PATH)
+        return _lib
+
+
+def lib_checked():
+    """The checked build (same ABI; device-side bounds checks compiled in),
+    loaded beside the normal library, with its signatures declared."""
+    global _lib_checked
+    with _lock:
+        if _lib_checked is None:
+            _lib_checked = _load(LIB_CHECKED_PATH)
+        return _lib_checked
+
+
+def _load(path: str):
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built; run dense_gemm_09_gb300.build()" % path)
+    L = ctypes.CDLL(path)
+    i64, f32, vp, ci = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
+    sig = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+    for name in ("gemm_f32", "gemm_tf32", "gemm_f16_tn", "gemm_f16_nn", "gemm_bf16_tn",
+                 "gemm_bf16_nn"):
+        fn = getattr(L, name)
+        fn.argtypes = sig
+        fn.restype = ci
+    L.dgemm_status_string.argtypes = [ci]
+    L.dgemm_status_string.restype = ctypes.c_char_p
+    L.dgemm_device_status.argtypes = [ci]
+    L.dgemm_device_status.restype = ci
+    L.dgemm_test_inject_stall.argtypes = [ctypes.c_uint64]
+    L.dgemm_test_inject_stall.restype = ci
+    L.dgemm_last_kernel.argtypes = []
+    L.dgemm_last_kernel.restype = ctypes.c_char_p
+    L.dgemm_tune_next.argtypes = [ci, ci, ci]
+    L.dgemm_tune_next.restype = ci
+    L.gemm_tf32_ws.argtypes = sig[:11] + [vp, i64, vp]
+    L.gemm_tf32_ws.restype = ci
+    L.gemm_f32_ws.argtypes = sig[:11] + [vp, i64, vp]
+    L.gemm_f32_ws.restype = ci
+    L.gemm_tf32_workspace_bytes.argtypes = [i64, i64, i64, vp, i64, vp, i64]
+    L.gemm_tf32_workspace_bytes.restype = i64
+    L.gemm_tf32_noalloc.argtypes = sig
+    L.gemm_tf32_noalloc.restype = ci
+    L.dgemm_test_pair_units.argtypes = [i64, i64, i64, i64, i64, vp, i64]
+    L.dgemm_test_pair_units.restype = i64
+    L.dgemm_test_stream_k_tiles.argtypes = [i64, i64, i64, ci, ci]
+    L.dgemm_test_stream_k_tiles.restype = i64
+    L.dgemm_test_choose_config.argtypes = [ci, i64, i64, i64, ci, vp, vp, vp]
+    L.dgemm_test_choose_config.restype = ci
+    L.dgemm_check_site.argtypes = []
+    L.dgemm_check_site.restype = ci
+    L.dgemm_test_shrink_bounds.argtypes = [i64]
+    L.dgemm_test_shrink_bounds.restype = ci
+    return L
 
 
 def status_string(status: int) -> str:

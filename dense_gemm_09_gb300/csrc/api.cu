@@ -64,6 +64,27 @@ int validate(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_
     return DGEMM_OK;
 }
 
+// The checked build's bounds-check words of every unit, combined: the first
+// nonzero status, and the site of that unit's first failed check.
+int checks_failed(int clear, int *site)
+{
+    int (*const readers[])(int, int *) = {check_status_simt, check_status_tma, check_status_umma,
+                                          check_status_scale, check_status_repack};
+    int status = DGEMM_OK, where = 0;
+    for (auto rd : readers) {
+        int s = 0;
+        const int st = rd(clear, &s);
+        if (st != DGEMM_OK && status == DGEMM_OK) {
+            status = st;
+            where = s;
+        }
+    }
+    if (site) *site = where;
+    return status;
+}
+
+thread_local int64_t t_shrink_rows = 0;
+
 int finish(const char *name)
 {
     if (!name) return DGEMM_ERR_LAUNCH;
@@ -261,6 +282,7 @@ extern "C" const char *dgemm_status_string(int status)
     case DGEMM_ERR_UNSUPPORTED_DEVICE: return "DGEMM_ERR_UNSUPPORTED_DEVICE: current device is not sm_103 (GB300)";
     case DGEMM_ERR_LAUNCH: return "DGEMM_ERR_LAUNCH: the CUDA runtime reported a launch error";
     case DGEMM_ERR_TIMEOUT: return "DGEMM_ERR_TIMEOUT: a kernel wait ran out and the kernel exited early";
+    case DGEMM_ERR_BOUNDS: return "DGEMM_ERR_BOUNDS: a device-side bounds check failed (checked build)";
     default: return "unknown dgemm status";
     }
 }
@@ -271,7 +293,35 @@ extern "C" int dgemm_device_status(int clear)
     int st = check_device(dev);
     if (st != DGEMM_OK) return st;
     if (cudaDeviceSynchronize() != cudaSuccess) return DGEMM_ERR_LAUNCH;
-    return umma_read_status(clear);
+    const int a = umma_read_status(clear);
+    const int b = simt_read_status(clear);
+    if (a != DGEMM_OK) return a;
+    if (b != DGEMM_OK) return b;
+    return checks_failed(clear, nullptr);
+}
+
+extern "C" int dgemm_check_site(void)
+{
+    DeviceInfo dev;
+    if (check_device(dev) != DGEMM_OK) return 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return 0;
+    int site = 0;
+    checks_failed(0, &site);
+    return site;
+}
+
+extern "C" int dgemm_test_shrink_bounds(int64_t rows)
+{
+    if (rows < 0) return DGEMM_ERR_INVALID_ARG;
+    t_shrink_rows = rows;
+    return DGEMM_OK;
+}
+
+int64_t dgemm::take_shrink_bounds()
+{
+    const int64_t v = t_shrink_rows;
+    t_shrink_rows = 0;
+    return v;
 }
 
 extern "C" int dgemm_tune_next(int variant, int bn, int split)

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace dgemm {
@@ -36,6 +37,39 @@ struct DeviceInfo {
 const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                               int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                               int64_t ldc, cudaStream_t stream, const DeviceInfo &dev);
+
+// FP32 SIMT path fed by TMA (A and B with 16-byte aligned bases and row
+// pitches; the caller checks that).  nullptr if it cannot be used for this
+// call (sizes beyond TMA's coordinates, a refused tensor map), in which case
+// nothing was launched.
+const char *launch_sgemm_tma(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                             const float *B, int64_t ldb, float beta, float *C, int64_t ldc, cudaStream_t stream);
+
+// Device status word of the TMA-fed SIMT kernel (see dgemm_device_status).
+int simt_read_status(int clear);
+
+// A 2-D tiled tensor map with zero fill out of range (false if the driver's
+// encoder is unavailable or refuses the description).
+bool encode_tiled_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+// The stall requested by dgemm_test_inject_stall for the next launch of a
+// kernel with bounded waits on this host thread (its wait limit in ns, 0 if
+// none); taking it clears the request.
+uint64_t take_injected_stall();
+
+// Each unit's checked-build words (checked.cuh): status 0 or
+// DGEMM_ERR_BOUNDS, *site the first failed check; reset when clear != 0.
+// Always 0 in the normal build.
+int check_status_simt(int clear, int *site);
+int check_status_tma(int clear, int *site);
+int check_status_umma(int clear, int *site);
+int check_status_scale(int clear, int *site);
+int check_status_repack(int clear, int *site);
+
+// Rows taken off M for the C-store checks of the next TMA-fed SIMT launch
+// on this host thread (dgemm_test_shrink_bounds); taking it clears it.
+int64_t take_shrink_bounds();
 
 // Tensor-core paths: operand kinds (TN = B stored N x K, NN = B stored K x N).
 enum UmmaKind { kUmmaF16TN = 0, kUmmaTF32NN = 1, kUmmaBF16TN = 2, kUmmaF16NN = 3, kUmmaBF16NN = 4 };

@@ -14,6 +14,9 @@
 
 #include "internal.h"
 
+#define DGEMM_UNIT 5
+#include "checked.cuh"
+
 namespace dgemm {
 namespace {
 
@@ -35,7 +38,8 @@ __global__ void __launch_bounds__(kRepackThreads)
             v.y = c + 1 < cols ? s[c + 1] : 0.f;
             v.z = c + 2 < cols ? s[c + 2] : 0.f;
             v.w = c + 3 < cols ? s[c + 3] : 0.f;
-            d[q] = v;
+            // the 16-byte store is aligned and stays inside the padded row
+            if (DGEMM_CHECK(c + 3 < ld_dst && (reinterpret_cast<uintptr_t>(d + q) & 15u) == 0)) d[q] = v;
         }
     }
 }
@@ -54,3 +58,5 @@ bool launch_repack_f32(const float *src, int64_t rows, int64_t cols, int64_t ld_
 }
 
 }  // namespace dgemm
+
+DGEMM_DEFINE_CHECK_READER(check_status_repack)

@@ -10,6 +10,9 @@
 
 #include "internal.h"
 
+#define DGEMM_UNIT 4
+#include "checked.cuh"
+
 namespace dgemm {
 namespace {
 
@@ -21,7 +24,7 @@ __global__ void scale_f32_kernel(int64_t M, int64_t N, float beta, float *__rest
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         float *row = C + m * ldc;
         for (int64_t n = threadIdx.x; n < N; n += blockDim.x)
-            row[n] = (beta == 0.f) ? 0.f : beta * row[n];
+            if (DGEMM_CHECK(n < ldc)) row[n] = (beta == 0.f) ? 0.f : beta * row[n];
     }
 }
 
@@ -31,7 +34,7 @@ __global__ void scale_f16_kernel(int64_t M, int64_t N, float beta, __half *__res
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         __half *row = C + m * ldc;
         for (int64_t n = threadIdx.x; n < N; n += blockDim.x)
-            row[n] = (beta == 0.f) ? __float2half_rn(0.f)
+            if (DGEMM_CHECK(n < ldc)) row[n] = (beta == 0.f) ? __float2half_rn(0.f)
                                    : __float2half_rn(beta * __half2float(row[n]));
     }
 }
@@ -42,7 +45,7 @@ __global__ void scale_bf16_kernel(int64_t M, int64_t N, float beta, __nv_bfloat1
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         __nv_bfloat16 *row = C + m * ldc;
         for (int64_t n = threadIdx.x; n < N; n += blockDim.x)
-            row[n] = (beta == 0.f) ? __float2bfloat16_rn(0.f)
+            if (DGEMM_CHECK(n < ldc)) row[n] = (beta == 0.f) ? __float2bfloat16_rn(0.f)
                                    : __float2bfloat16_rn(beta * __bfloat162float(row[n]));
     }
 }
@@ -78,3 +81,5 @@ const char *launch_scale_bf16(int64_t M, int64_t N, float beta, uint16_t *C, int
 }
 
 }  // namespace dgemm
+
+DGEMM_DEFINE_CHECK_READER(check_status_scale)

@@ -43,6 +43,9 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+#define DGEMM_UNIT 1
+#include "checked.cuh"
+
 namespace dgemm {
 namespace {
 
@@ -105,7 +108,8 @@ __device__ __forceinline__ void load_slice(uint32_t stage_smem, const float *__r
         const int64_t gm = m0 + m, gk = k0 + k;
         const bool ok = gm < M && gk < K;
         const float *src = ok ? A + gm * lda + gk : A;
-        cp_async4(as + static_cast<uint32_t>((k * AS_LD + m) * 4), src, ok ? 4u : 0u);
+        if (DGEMM_CHECK(m < BM && k < BK))  // the transposed slot lies inside As
+            cp_async4(as + static_cast<uint32_t>((k * AS_LD + m) * 4), src, ok ? 4u : 0u);
     }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -113,6 +117,7 @@ __device__ __forceinline__ void load_slice(uint32_t stage_smem, const float *__r
         const int n = lane * 4;
         const int64_t gk = k0 + k, gn = n0 + n;
         const uint32_t dst = bs + static_cast<uint32_t>((k * BN + n) * 4);
+        if (!DGEMM_CHECK(k < BK && n + 3 < BN)) continue;  // the four slots lie inside Bs
         if constexpr (kVec) {
             const int64_t left = gk < K ? N - gn : 0;
             const uint32_t bytes = left >= 4 ? 16u : (left > 0 ? static_cast<uint32_t>(left) * 4u : 0u);
@@ -133,7 +138,7 @@ __device__ __forceinline__ void epilogue_store(float *__restrict__ C, int64_t ld
 {
     if (gm >= M) return;
     float *p = C + gm * ldc + gn;
-    if (vec_c && gn + 3 < N) {
+    if (vec_c && gn + 3 < N && DGEMM_CHECK((reinterpret_cast<uintptr_t>(p) & 15u) == 0)) {
         float4 o;
         o.x = alpha * acc[0];
         o.y = alpha * acc[1];
@@ -200,6 +205,8 @@ __device__ __forceinline__ void split_reduce_store(const float2 (&acc)[8][4], ui
         if (owner == rank) continue;
         const uint32_t slot = rank < owner ? rank : rank - 1;
         const uint32_t off = split_recv_offset(slot, static_cast<uint32_t>(i) / S, 0, S, tid);
+        // both 16-byte words land inside the owner's stage ring
+        if (!DGEMM_CHECK(owner < S && off + THREADS * 16 + 16 <= static_cast<uint32_t>(SMEM_BYTES))) continue;
         const uint32_t dst = ptx::mapa(smem0 + off, owner);
         ptx::st_shared_cluster_v4(dst, make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y));
         ptx::st_shared_cluster_v4(dst + THREADS * 16,
@@ -218,8 +225,12 @@ __device__ __forceinline__ void split_reduce_store(const float2 (&acc)[8][4], ui
             } else {
                 const uint32_t slot = q < rank ? q : q - 1;
                 const uint32_t off = split_recv_offset(slot, static_cast<uint32_t>(i) / S, 0, S, tid);
-                l = ptx::ld_shared_v4f(smem0 + off);
-                h = ptx::ld_shared_v4f(smem0 + off + THREADS * 16);
+                if (DGEMM_CHECK(off + THREADS * 16 + 16 <= static_cast<uint32_t>(SMEM_BYTES))) {
+                    l = ptx::ld_shared_v4f(smem0 + off);
+                    h = ptx::ld_shared_v4f(smem0 + off + THREADS * 16);
+                } else {
+                    l = h = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
             lo[0] += l.x; lo[1] += l.y; lo[2] += l.z; lo[3] += l.w;
             hi[0] += h.x; hi[1] += h.y; hi[2] += h.z; hi[3] += h.w;
@@ -290,8 +301,11 @@ __global__ void __launch_bounds__(THREADS, 2)
     // (the host splits only when kt_count < 2^28, so 32-bit products suffice)
     constexpr bool kMaySplit = kMode != kPlain;
     const int64_t kt0 = kMaySplit ? static_cast<int64_t>(rank * static_cast<uint32_t>(kt_count) / S) : 0;
-    const int64_t kt1 =
-        kMaySplit ? static_cast<int64_t>((rank + 1) * static_cast<uint32_t>(kt_count) / S) : kt_count;
+    int64_t kt1 = kMaySplit ? static_cast<int64_t>((rank + 1) * static_cast<uint32_t>(kt_count) / S) : kt_count;
+    // the raster maps the CTA onto a tile inside C, and the thread's fragment
+    // columns (ty * 4 .. ty * 4 + 67, tx * 4 .. tx * 4 + 67) lie inside the
+    // slice rows; otherwise the CTA loads and stores nothing
+    if (!DGEMM_CHECK_CTA(m0 >= 0 && m0 < M && n0 >= 0 && n0 < N && ty < 16 && tx < 16)) kt1 = kt0;
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
         if (kt0 + s < kt1)
@@ -476,6 +490,19 @@ const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, cons
     // 16-byte copies of B need a 16-byte aligned base and row pitch.
     const bool vec_b = aligned16(B) && (ldb % 4 == 0);
     const bool vec_c = aligned16(C) && (ldc % 4 == 0);
+    // Problems of at least a wave of tiles whose A and B TMA can describe
+    // take the TMA-fed kernel (sgemm_tma.cu).
+    if (vec_b && aligned16(A) && (lda % 4 == 0)) {
+        int device = 0;
+        cudaGetDevice(&device);
+        const SimtOccupancy &occ = occupancy<true>(device);
+        const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+        if (plan_simt(tiles, (K + BK - 1) / BK, static_cast<int64_t>(occ.blocks_per_sm) * dev.sm_count, occ).mode ==
+            kPlain) {
+            if (const char *name = launch_sgemm_tma(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
+                return name;
+        }
+    }
     SimtPlan pl{kPlain, 1};
     const bool ok =
         vec_b ? launch_kernel<true>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, vec_c, stream, dev, pl)
@@ -487,3 +514,5 @@ const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, cons
 }
 
 }  // namespace dgemm
+
+DGEMM_DEFINE_CHECK_READER(check_status_simt)

@@ -55,6 +55,9 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+#define DGEMM_UNIT 3
+#include "checked.cuh"
+
 namespace dgemm {
 
 __device__ int g_umma_status;
@@ -431,7 +434,8 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u) {
                     const int idx = ptid + (i0 + u) * 128;
-                    st_shared(sa + sw128_offset(idx / BK, (idx % BK) * sizeof(E)), v[u]);
+                    const uint32_t off = sw128_offset(idx / BK, (idx % BK) * sizeof(E));
+                    if (DGEMM_CHECK(off + sizeof(E) <= static_cast<uint32_t>(A_TILE_BYTES))) st_shared(sa + off, v[u]);
                 }
             }
             // B tile, staged K-major: row n holds BK consecutive k.
@@ -453,7 +457,8 @@ __device__ __forceinline__ void run_reg_producer(const Params &p, uint32_t smem_
                     const int idx = ptid + (i0 + u) * 128;
                     const int n = !T::kBNMajor ? idx / BK : idx % BN;
                     const int k = !T::kBNMajor ? idx % BK : idx / BN;
-                    st_shared(sb + sw128_offset(n, k * sizeof(E)), v[u]);
+                    const uint32_t off = sw128_offset(n, k * sizeof(E));
+                    if (DGEMM_CHECK(off + sizeof(E) <= static_cast<uint32_t>(B_TILE_BYTES))) st_shared(sb + off, v[u]);
                 }
             }
             ptx::fence_proxy_async_smem();
@@ -518,7 +523,8 @@ __device__ __forceinline__ void run_cpasync_producer(const Params &p, uint32_t s
                 const int r = idx / BK, c = idx % BK;
                 const int64_t gm = m0 + r, gk = k0 + c;
                 const bool in = gm < p.M && gk < p.K;
-                cp_async4_zfill(sa + sw128_offset(r, c * 4), in ? A + gm * p.lda + gk : A, in);
+                if (DGEMM_CHECK(sw128_offset(r, c * 4) + 4 <= static_cast<uint32_t>(A_TILE_BYTES)))
+                    cp_async4_zfill(sa + sw128_offset(r, c * 4), in ? A + gm * p.lda + gk : A, in);
             }
             // B tile (stored K x N): consecutive threads take consecutive n;
             // staged K-major (row n holds BK consecutive k)
@@ -528,7 +534,8 @@ __device__ __forceinline__ void run_cpasync_producer(const Params &p, uint32_t s
                 const int n = idx % BN, k = idx / BN;
                 const int64_t gn = n0 + n, gk = k0 + k;
                 const bool in = gn < p.N && gk < p.K;
-                cp_async4_zfill(sb + sw128_offset(n, k * 4), in ? B + gk * p.ldb + gn : B, in);
+                if (DGEMM_CHECK(sw128_offset(n, k * 4) + 4 <= static_cast<uint32_t>(B_TILE_BYTES)))
+                    cp_async4_zfill(sb + sw128_offset(n, k * 4), in ? B + gk * p.ldb + gn : B, in);
             }
             ptx::cp_async_commit_group();
             pending[npending++] = stage;
@@ -627,7 +634,7 @@ __device__ __forceinline__ void store_chunk(const Params &p, int64_t row, int64_
     const float alpha = p.alpha, beta = p.beta;
     if constexpr (T::kElem == 2) {
         uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + row * p.ldc;
-        if (p.vec_c && col + 31 < p.N) {
+        if (p.vec_c && col + 31 < p.N && DGEMM_CHECK((reinterpret_cast<uintptr_t>(crow + col) & 15u) == 0)) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint4 *dst = reinterpret_cast<uint4 *>(crow + col + q * 8);
@@ -659,7 +666,7 @@ __device__ __forceinline__ void store_chunk(const Params &p, int64_t row, int64_
         }
     } else {
         float *crow = reinterpret_cast<float *>(p.C) + row * p.ldc;
-        if (p.vec_c && col + 31 < p.N) {
+        if (p.vec_c && col + 31 < p.N && DGEMM_CHECK((reinterpret_cast<uintptr_t>(crow + col) & 15u) == 0)) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 float4 *dst = reinterpret_cast<float4 *>(crow + col + q * 4);
@@ -719,7 +726,7 @@ __device__ __forceinline__ void load_old(const Params &p, int64_t row, int64_t c
     if constexpr (Traits<kKind>::kElem == 2) {
         constexpr bool kBF = Traits<kKind>::kBF;
         const uint16_t *crow = reinterpret_cast<const uint16_t *>(p.C) + row * p.ldc;
-        if (p.vec_c && col + COLS - 1 < p.N) {
+        if (p.vec_c && col + COLS - 1 < p.N && DGEMM_CHECK((reinterpret_cast<uintptr_t>(crow + col) & 15u) == 0)) {
 #pragma unroll
             for (int q = 0; q < COLS / 8; ++q) {
                 const uint4 u = *reinterpret_cast<const uint4 *>(crow + col + q * 8);
@@ -738,7 +745,7 @@ __device__ __forceinline__ void load_old(const Params &p, int64_t row, int64_t c
         }
     } else {
         const float *crow = reinterpret_cast<const float *>(p.C) + row * p.ldc;
-        if (p.vec_c && col + COLS - 1 < p.N) {
+        if (p.vec_c && col + COLS - 1 < p.N && DGEMM_CHECK((reinterpret_cast<uintptr_t>(crow + col) & 15u) == 0)) {
 #pragma unroll
             for (int q = 0; q < COLS / 4; ++q) {
                 const float4 f = *reinterpret_cast<const float4 *>(crow + col + q * 4);
@@ -776,7 +783,7 @@ __device__ __forceinline__ void store_chunk_by_rows(const Params &p, int64_t row
 #pragma unroll 4
     for (int i = 0; i < 32; ++i) {
         const int64_t row = row0 + i;
-        if (row >= p.M) break;  // warp-uniform
+        if (row >= p.M || !DGEMM_CHECK(row >= 0)) break;  // warp-uniform
         const uint32_t u = ptx::ld_shared_b32(smem + (static_cast<uint32_t>(i) * 32u + (lane ^ static_cast<uint32_t>(i))) * 4u);
         if (c < p.N) {
             float v = p.alpha * __uint_as_float(u);
@@ -806,6 +813,8 @@ __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *t
 {
     if (cols == 0) cols = p.bn;
     const int64_t row = row0 + lane;
+    // the warp's TMEM columns lie inside the 512 allocated (warp-uniform)
+    if (!DGEMM_CHECK((taddr & 0xFFFFu) + static_cast<uint32_t>(cols) <= static_cast<uint32_t>(TMEM_COLS))) return;
     if (!p.tma_store) {
 #pragma unroll 1
         for (int c = 0; c < cols / 32; ++c) {
@@ -844,6 +853,7 @@ __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *t
         if (lane == 0 && nbox >= kBoxes) ptx::bulk_wait_read<kBoxes - 1>();  // this box's last store read it
         __syncwarp();
         const uint32_t rowbase = buf + static_cast<uint32_t>(lane) * 128u;
+        if (!DGEMM_CHECK(lane < 32 && (nbox % kBoxes) < static_cast<uint32_t>(kBoxes))) continue;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             uint4 q;
@@ -859,7 +869,8 @@ __device__ __forceinline__ void drain_rows(const Params &p, const CUtensorMap *t
         }
         ptx::fence_proxy_async_smem();  // make the box visible to the TMA engine
         __syncwarp();
-        if (lane == 0) {
+        // a TMA store starts at non-negative coordinates inside C
+        if (lane == 0 && DGEMM_CHECK(row0 >= 0 && col0 >= 0 && row0 < p.M && col0 < p.N)) {
             ptx::tma_store_2d(tmap_c, buf, static_cast<int32_t>(col0), static_cast<int32_t>(row0));
             ptx::bulk_commit();
         }
@@ -884,8 +895,10 @@ __device__ __forceinline__ void run_epilogue(const Params &p, const CUtensorMap 
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + acc * BN;
-        drain_rows<kKind>(p, tmap_c, taddr, m0 + quarter * 32, n0,
-                          epi_smem + quarter * 2 * EPI_BOX_BYTES, lane, nbox);
+        // the schedule's tile lies inside C (warp-uniform)
+        if (DGEMM_CHECK(m0 >= 0 && m0 < p.M && n0 >= 0 && n0 < p.N))
+            drain_rows<kKind>(p, tmap_c, taddr, m0 + quarter * 32, n0,
+                              epi_smem + quarter * 2 * EPI_BOX_BYTES, lane, nbox);
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_addr(&ctrl->tmem_empty[acc]));
         acc ^= 1u;
@@ -959,6 +972,10 @@ __device__ __forceinline__ void splitk_push(const Params &p, uint32_t tmem_base,
         ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
         ptx::tmem_ld_wait();
         const uint32_t slot = rank < owner ? rank : rank - 1;
+        // the eight 16-byte words land inside the owner's stage ring
+        if (!DGEMM_CHECK(owner < S && recv_offset(slot, static_cast<uint32_t>(c) / S, S, 7, row) + 16 <=
+                                          static_cast<uint32_t>(STAGES * STAGE_BYTES)))
+            continue;
         const uint32_t base = ptx::mapa(smem_base + recv_offset(slot, static_cast<uint32_t>(c) / S, S, 0, row),
                                         owner);
 #pragma unroll
@@ -998,6 +1015,8 @@ __device__ __forceinline__ void splitk_reduce(const Params &p, uint32_t tmem_bas
             } else {
                 const uint32_t slot = q < rank ? q : q - 1;
                 const uint32_t base = smem_base + recv_offset(slot, c / S, S, 0, row);
+                if (!DGEMM_CHECK(recv_offset(slot, c / S, S, 7, row) + 16 <= static_cast<uint32_t>(STAGES * STAGE_BYTES)))
+                    continue;
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
                     const float4 f = ptx::ld_shared_v4f(base + static_cast<uint32_t>(v) * BM * 16u);
@@ -1280,6 +1299,8 @@ struct WorkIter {
 // access is 512 contiguous bytes.  One flag per region.
 constexpr int SK_WARP_SLOTS = 8;
 constexpr int64_t SK_REGION_FLOATS = 32 * 256;
+constexpr int SK_MAX_PAIRS = 128;  // pair slots of the static workspace
+constexpr int64_t SK_REGIONS = static_cast<int64_t>(SK_MAX_PAIRS) * 2 * SK_WARP_SLOTS;
 
 __device__ __forceinline__ int64_t sk_region(int64_t slot, uint32_t half, int w)
 {
@@ -1292,6 +1313,7 @@ __device__ __forceinline__ int64_t sk_region(int64_t slot, uint32_t half, int w)
 __device__ __forceinline__ void sk_publish(const Params &p, uint32_t taddr, int cols, int64_t region,
                                           int lane)
 {
+    if (!DGEMM_CHECK(region >= 0 && region < SK_REGIONS && cols <= 256)) return;  // warp-uniform
     float4 *dst = reinterpret_cast<float4 *>(p.sk_work + region * SK_REGION_FLOATS);
 #pragma unroll 1
     for (int c = 0; c < cols / 32; ++c) {
@@ -1309,6 +1331,7 @@ __device__ __forceinline__ void sk_publish(const Params &p, uint32_t taddr, int 
 // Stamp the region's flag once every lane's stores are visible (release).
 __device__ __forceinline__ void sk_flag(const Params &p, int64_t region, int lane)
 {
+    if (!DGEMM_CHECK(region >= 0 && region < SK_REGIONS)) return;  // warp-uniform
     __threadfence();
     __syncwarp();
     if (lane == 0) ptx::st_release_gpu_u64(p.sk_flags + region, p.sk_gen);
@@ -1319,6 +1342,7 @@ __device__ __forceinline__ void sk_flag(const Params &p, int64_t region, int lan
 // loads do not go to HBM.
 __device__ __forceinline__ void sk_prefetch(const Params &p, int cols, int64_t region, int lane)
 {
+    if (!DGEMM_CHECK(region >= 0 && region < SK_REGIONS)) return;
     const bool ready = ptx::ld_acquire_gpu_u64(p.sk_flags + region) == p.sk_gen;
     if (!ready) return;
     const char *base = reinterpret_cast<const char *>(p.sk_work + region * SK_REGION_FLOATS);
@@ -1333,6 +1357,9 @@ __device__ __forceinline__ bool sk_init(const Params &p, uint32_t taddr, int64_t
 {
     constexpr int kChunks = BN / 32;
     static_assert(kChunks % 2 == 0, "chunks are loaded in pairs");
+    // a region of the workspace, and TMEM columns inside the allocation (warp-uniform)
+    if (!DGEMM_CHECK(region >= 0 && region < SK_REGIONS && (taddr & 0xFFFFu) + BN <= static_cast<uint32_t>(TMEM_COLS)))
+        return false;
     bool ok = true;
     if (lane == 0) {
         const uint64_t *flag = p.sk_flags + region;
@@ -1590,7 +1617,9 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
-        if (u.publish)
+        if (!DGEMM_CHECK(m0 >= 0 && m0 < p.M && n0 >= 0 && n0 < p.N && static_cast<uint32_t>(slot) < 8u)) {
+            // (the schedule's tile lies inside C; nothing is drained otherwise)
+        } else if (u.publish)
             sk_publish(p, taddr, BN, sk_region(cluster, rank & 1u, slot), lane);
         else if constexpr (kWide == 2)
             drain_rows<kKind, 1>(p, tmap_c, taddr, m0 + (rank & 1u) * 128 + quarter * 32,
@@ -1787,8 +1816,6 @@ int pair_clusters()
 // Stream-K is not used while the stream is being captured into a graph (the
 // graph would hold the shared workspace); the round-robin schedule then
 // runs, with bit-identical results.
-constexpr int SK_MAX_PAIRS = 128;
-constexpr int64_t SK_REGIONS = static_cast<int64_t>(SK_MAX_PAIRS) * 2 * SK_WARP_SLOTS;
 __device__ __align__(256) float g_sk_work[SK_REGIONS * SK_REGION_FLOATS];
 __device__ uint64_t g_sk_flags[SK_REGIONS];
 
@@ -1939,10 +1966,10 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, 
     p.sk_gen = 0;
     p.stages = STAGES;
     p.stage_bytes = STAGE_BYTES;
-    p.inject_stall = t_inject_limit_ns ? 1 : 0;
+    const uint64_t stall = take_injected_stall();
+    p.inject_stall = stall ? 1 : 0;
     p.splitk = 1;
-    p.wait_limit_ns = t_inject_limit_ns ? t_inject_limit_ns : kWaitLimitNs;
-    t_inject_limit_ns = 0;
+    p.wait_limit_ns = stall ? stall : kWaitLimitNs;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -2418,6 +2445,19 @@ void umma_inject_stall(uint64_t wait_limit_ns)
     t_inject_limit_ns = wait_limit_ns ? wait_limit_ns : 1;
 }
 
+uint64_t take_injected_stall()
+{
+    const uint64_t v = t_inject_limit_ns;
+    t_inject_limit_ns = 0;
+    return v;
+}
+
+bool encode_tiled_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle)
+{
+    return make_map(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, swizzle);
+}
+
 int umma_read_status(int clear)
 {
     int v = 0;
@@ -2431,3 +2471,5 @@ int umma_read_status(int clear)
 }
 
 }  // namespace dgemm
+
+DGEMM_DEFINE_CHECK_READER(check_status_umma)

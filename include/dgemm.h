@@ -38,8 +38,12 @@
  *   the workspace, so results are bit-identical to uncut tiles.  Launches
  *   that use the workspace are ordered one after another across streams
  *   through an event (the library records it and makes the next such launch
- *   wait on it); under stream capture the calls do not cut tiles.  Source:
- *   none on the pages (their kernels deal whole tiles).
+ *   wait on it); under stream capture the calls do not cut tiles.  So two
+ *   tensor-core calls on different, otherwise independent streams do not
+ *   overlap on the GPU when both cut tiles: the one issued second starts
+ *   after the first has finished (each result is still exact).  Calls that
+ *   do not cut tiles, and gemm_f32, are not ordered this way.  Source: none
+ *   on the pages (their kernels deal whole tiles).
  * Special cases (BLAS conventions):
  *   M == 0 or N == 0  -> DGEMM_OK, nothing is launched;
  *   K == 0 or alpha == 0 -> C = beta * C, A and B are never read; with
@@ -78,7 +82,8 @@ typedef enum {
     DGEMM_ERR_INVALID_ARG = 1,
     DGEMM_ERR_UNSUPPORTED_DEVICE = 2,
     DGEMM_ERR_LAUNCH = 3,
-    DGEMM_ERR_TIMEOUT = 4
+    DGEMM_ERR_TIMEOUT = 4,
+    DGEMM_ERR_BOUNDS = 5  /* checked build only: a device-side bounds check failed */
 } dgemm_status;
 
 /*
@@ -103,6 +108,8 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha,
  * products run on the tensor cores in TF32 (each FP32 operand is reduced to
  * 1+8+10 bits inside the multiplier; the stored A and B are not modified),
  * with FP32 accumulation and an FP32 alpha/beta epilogue.
+ * Large problems may take the stream-K schedule (see "Stream-K" above:
+ * such calls are ordered across streams).
  * Source: "SGEMM CUDA代码学习", section "第 5 步" (TF32 tensor cores: a
  * 19-bit float, 1+8+10) and its WMMA TF32 multi-stage kernel.
  */
@@ -254,20 +261,58 @@ const char *dgemm_status_string(int status);
 
 /*
  * dgemm_device_status -- read (and, if clear != 0, reset) the current
- * device's kernel status word.  The tensor-core kernels bound every wait on
- * an mbarrier; a wait that runs out records DGEMM_ERR_TIMEOUT here and the
- * kernel exits cleanly instead of hanging.  This call synchronises the
+ * device's kernel status word.  The tensor-core kernels and the TMA-fed
+ * FP32 SIMT kernel bound every wait on an mbarrier; a wait that runs out
+ * records DGEMM_ERR_TIMEOUT here and the kernel exits cleanly instead of
+ * hanging.  This call synchronises the
  * device.  Returns DGEMM_OK when no kernel has recorded an error since the
  * last clear.  Source: none on the pages (they never check kernels).
  */
 int dgemm_device_status(int clear);
 
 /*
+ * The checked build.  The library is also built as libdgemm_checked.so,
+ * with the same ABI, compiled with -DDGEMM_CHECKED: every kernel then tests
+ * the indices it computes -- shared-memory offsets (stage rings, swizzled
+ * rows, epilogue boxes, split-K receive buffers), tile coordinates, global
+ * rows and columns of A, B and C, the alignment of 16-byte accesses, TMEM
+ * columns and stream-K workspace regions -- against the extents they must
+ * stay inside.  A failed check skips the access it guards (no trap, nothing
+ * out of bounds) and records DGEMM_ERR_BOUNDS in the device status (see
+ * dgemm_device_status) and its site.  The checks cost time and are meant for
+ * testing; in libdgemm.so they are compiled out.
+ *
+ * dgemm_check_site -- the site of the first failed check since the last
+ * clear of the device status: (translation unit x 100000 + source line) of
+ * the library's sources, units 1 sgemm_simt.cu, 2 sgemm_tma.cu,
+ * 3 umma_gemm.cu, 4 scale_c.cu, 5 repack.cu; 0 if none failed, and always 0
+ * in libdgemm.so.  Synchronises the device.  Source: none on the pages.
+ */
+int dgemm_check_site(void);
+
+/*
+ * dgemm_test_shrink_bounds -- TEST HOOK for the checked build.  The next
+ * gemm_f32 launch of the TMA-fed SIMT kernel made by the calling host thread
+ * checks its stores against M - rows rows of C instead of M, so that the
+ * stores to the last `rows` rows fail their check: they are skipped and
+ * reported (DGEMM_ERR_BOUNDS, a site in sgemm_tma.cu).  This shows that the
+ * checks are live without any out-of-bounds access.  In libdgemm.so the
+ * request is taken by the same launch and has no effect.  rows < 0 is
+ * DGEMM_ERR_INVALID_ARG; otherwise returns DGEMM_OK.  Source: none on the
+ * pages.
+ */
+int dgemm_test_shrink_bounds(int64_t rows);
+
+/*
  * dgemm_test_inject_stall -- TEST HOOK, not for applications.  Arms a one-shot
- * fault for the next gemm_tf32 / gemm_f16_tn launch made by the calling host
- * thread: its MMA issuer first waits on a barrier that nothing arrives at,
- * and every wait of that launch is bounded by wait_limit_ns (0 means 1 ns) instead of
- * the default 4 s.  The launch then ends by itself, with DGEMM_ERR_TIMEOUT in
+ * fault for the next launch, made by the calling host thread, of a kernel
+ * with bounded waits: a tensor-core kernel (gemm_tf32, the 16-bit calls) or
+ * the TMA-fed FP32 SIMT kernel (gemm_f32 on aligned operands of at least a
+ * wave of tiles).  That launch first waits on a barrier that nothing
+ * arrives at (in the MMA issuer, or in every warp of the SIMT kernel), and
+ * every wait of that launch is bounded by wait_limit_ns (0 means 1 ns)
+ * instead of the default 4 s.  Calls that launch other kernels leave the
+ * request armed.  The launch then ends by itself, with DGEMM_ERR_TIMEOUT in
  * the device status word (see dgemm_device_status) and C left unspecified;
  * the CUDA context stays usable.  Always returns DGEMM_OK.  Source: none on
  * the pages (they have no failure detection).

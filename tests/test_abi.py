@@ -41,6 +41,18 @@ def test_every_declared_symbol_is_exported(L):
         assert getattr(L, name) is not None
 
 
+def test_checked_build_exports_the_same_symbols(L):
+    # the checked build (device-side bounds checks) has the same ABI
+    import dense_gemm_09_gb300 as dg
+    out = subprocess.check_output(["nm", "-D", "--defined-only", dg.LIB_CHECKED_PATH], text=True)
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+    Lc = dg.lib_checked()
+    assert Lc.dgemm_test_shrink_bounds(-1) == 1   # DGEMM_ERR_INVALID_ARG
+    assert Lc.dgemm_test_shrink_bounds(0) == 0
+
+
 def test_header_compiles_as_c(tmp_path):
     src = tmp_path / "t.c"
     src.write_text('#include "dgemm.h"\nint main(void){return gemm_f32(0,0,0,1.f,0,0,0,0,0.f,0,0,0);}\n')
@@ -50,7 +62,7 @@ def test_header_compiles_as_c(tmp_path):
 
 def test_status_strings(L):
     import dense_gemm_09_gb300 as dg
-    for code in range(5):
+    for code in range(6):
         s = dg.status_string(code)
         assert s.startswith("DGEMM_"), s
     assert "unknown" in dg.status_string(99)

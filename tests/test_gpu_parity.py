@@ -377,8 +377,8 @@ SIMT_SPLIT_CASES = [
     ((300, 520, 4100), "sgemm_simt_splitk8_"),         # 15 tiles, K tail in the last range
     ((127, 12288, 640), "sgemm_simt_splitk3_"),        # 96 tiles, skinny
     ((1200, 1300, 600), "sgemm_simt_splitk2_"),        # 110 tiles
-    ((2048, 2048, 64), "sgemm_simt_128x128"),          # 256 tiles, K too short to split
-    ((4092, 4092, 512), "sgemm_simt_128x128"),         # more tiles than one wave: no split
+    ((2048, 2048, 64), "sgemm_simt_tma_"),             # 256 tiles, K too short to split (TMA-fed)
+    ((4092, 4092, 512), "sgemm_simt_tma_"),            # more tiles than one wave: no split (TMA-fed)
 ]
 
 
@@ -419,6 +419,50 @@ def test_simt_split_unaligned_b():
     got, _, _ = parity.run("f32", A, B, C, 1.5, -0.25, pad=(0, 2, 0))
     assert dg.last_kernel().startswith("sgemm_simt_splitk") and dg.last_kernel().endswith("cpasync4")
     assert parity.worst_ratio("f32", got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+# FP32 SIMT fed by TMA: problems of at least a wave of tiles whose A and B
+# have 16-byte aligned bases and pitches.  Tails in M, N and K come from TMA's
+# zero fill and the epilogue's masks; a C pitch that is not a multiple of 4
+# takes the scalar stores.
+SIMT_TMA_CASES = [
+    ((2049, 2561, 1001), (3, 3, 0)),   # M, N, K tails; lda 1004, ldb 2564; C pitch 2561
+    ((2100, 2500, 37), (3, 0, 0)),     # K = 37: one partial K slice
+    ((2176, 2304, 96), (0, 0, 4)),     # whole tiles; padded C
+    ((4092, 4092, 512), (0, 0, 0)),    # the 4092 workload's shape with a shorter K
+]
+
+
+@pytest.mark.parametrize("shape,pad", SIMT_TMA_CASES)
+def test_simt_tma_kernel_matches_oracle(shape, pad):
+    import dense_gemm_09_gb300 as dg
+    M, N, K = shape
+    A, B, C = parity.host_operands("f32", M, N, K, seed=M + N + 7 * K)
+    got, _, _ = parity.run("f32", A, B, C, 1.5, -0.25, pad=pad)
+    assert dg.last_kernel().startswith("sgemm_simt_tma_"), dg.last_kernel()
+    assert parity.worst_ratio("f32", got, A, B, C, 1.5, -0.25) <= 1.0
+
+
+def test_simt_tma_kernel_is_bit_identical_to_cp_async_kernel():
+    # the same FMAs in the same order: A with an odd pitch takes the cp.async
+    # kernel, the aligned copy the TMA-fed one
+    import dense_gemm_09_gb300 as dg
+    M, N, K = 2100, 2400, 700
+    A, B, C = parity.host_operands("f32", M, N, K, seed=77)
+    tma, _, _ = parity.run("f32", A, B, C, 0.75, 0.5)
+    assert dg.last_kernel().startswith("sgemm_simt_tma_"), dg.last_kernel()
+    cpa, _, _ = parity.run("f32", A, B, C, 0.75, 0.5, pad=(1, 0, 0))
+    assert dg.last_kernel().startswith("sgemm_simt_128x128"), dg.last_kernel()
+    assert torch.equal(tma, cpa)
+
+
+def test_simt_tma_integers_bit_exact():
+    import dense_gemm_09_gb300 as dg
+    A, B, C = parity.host_operands("f32", 2304, 2176, 1028, seed=38, dist="int")
+    got, _, _ = parity.run("f32", A, B, C, 1.0, 2.0)
+    assert dg.last_kernel().startswith("sgemm_simt_tma_"), dg.last_kernel()
+    ref, _ = parity.reference("f32", A, B, C, 1.0, 2.0)
+    assert np.array_equal(got.double().numpy(), ref)
 
 
 # The tuning hook: every tile configuration the sweep tool can request gives

@@ -134,6 +134,31 @@ def test_stream_k_launches_on_several_streams():
         assert torch.equal(o, want)
 
 
+def test_stream_k_on_two_streams_matches_oracle():
+    """Two different stream-K problems (TF32 and FP16 TN) issued back to back
+    on two independent streams: the library orders them through its event
+    (they share the workspace), and each result agrees with the oracle."""
+    import dense_gemm_09_gb300 as dg
+    probs = []
+    for path, seed in (("tf32", 21), ("f16_tn", 22)):
+        M, N, K = 2500, 4500, 1000
+        A, B, C = parity.host_operands(path, M, N, K, seed=seed)
+        probs.append((path, A, B, C, A.cuda(), B.cuda(), C.cuda()))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    names = []
+    for (path, _, _, _, dA, dB, dC), s in zip(probs, streams):
+        with torch.cuda.stream(s):
+            dg.tune_next(dg.TUNE_PAIR_WIDE, 256, dg.SK_ON)
+            parity.fn(path)(dA, dB, dC, 0.75, 0.5)
+            names.append(dg.last_kernel())
+    torch.cuda.synchronize()
+    assert all("_sk_" in n for n in names), names
+    assert dg.device_status() == dg.OK
+    for path, A, B, C, _, _, dC in probs:
+        assert parity.worst_ratio(path, dC.cpu(), A, B, C, 0.75, 0.5) <= 1.0
+
+
 def test_stream_k_stall_times_out_cleanly():
     """A stalled stream-K launch: the MMA waits run out, the pairs waiting for
     a partial give up within their own limit, and the next launch (a new

@@ -1,7 +1,8 @@
 """Failure detection on the GPU without a fault: the bounded mbarrier waits.
 
-A test-only hook makes the next tensor-core launch's MMA issuer wait on a
-barrier nothing arrives at, so its wait (and then every other role's) runs
+A test-only hook makes the next launch of a kernel with bounded waits (the
+tensor-core kernels and the TMA-fed FP32 SIMT kernel) first wait on a
+barrier nothing arrives at, so that wait (and then every other role's) runs
 out after a short limit.  The kernel must end by itself, record
 DGEMM_ERR_TIMEOUT in the device status word, release its resources, and leave
 the context usable: the next ordinary call is correct."""
@@ -23,6 +24,7 @@ CASES = [
     ("tf32", (100, 260, 36), (1, 0, 0), None, "_cpasync"),    # cp.async producer (unaligned TF32)
     ("f16_tn", (100, 260, 36), (1, 0, 0), None, "_ldst"),     # register-path producer (unaligned FP16)
     ("f16_tn", (100, 1000, 2048), (0, 0, 0), None, "_splitk"),  # split-K cluster kernel
+    ("f32", (2048, 2560, 256), (0, 0, 0), None, "sgemm_simt_tma_"),  # TMA-fed FP32 SIMT kernel
 ]
 
 
@@ -37,7 +39,7 @@ def test_stalled_launch_times_out_cleanly(path, shape, pad, force, variant):
     dC = C.cuda()
     torch.cuda.synchronize()
     assert dg.device_status(clear=True) == dg.OK
-    fn = {"tf32": dg.gemm_tf32, "f16_tn": dg.gemm_f16_tn}[path]
+    fn = {"tf32": dg.gemm_tf32, "f16_tn": dg.gemm_f16_tn, "f32": dg.gemm_f32}[path]
 
     if force == "pair":
         dg.tune_next(dg.TUNE_PAIR)

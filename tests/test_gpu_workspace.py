@@ -147,7 +147,8 @@ def test_f32_ws_matches_oracle_and_plain_call(M, N, K, pad, offset):
     got = C.cuda()
     dg.gemm_f32_ws(dA, dB, got, 1.5, -0.25, workspace=ws)
     torch.cuda.synchronize()
-    assert dg.last_kernel().endswith("cpasync16"), dg.last_kernel()  # B now loads in 16-byte pieces
+    # B now loads in 16-byte pieces (or by TMA, when A allows it too)
+    assert not dg.last_kernel().endswith("cpasync4"), dg.last_kernel()
     assert parity.worst_ratio("f32", got.cpu(), A, B, C, 1.5, -0.25) <= 1.0
     # the same FP32 FMAs in the same order as the plain call on the same values
     want = C.cuda()
