@@ -88,7 +88,7 @@ FAMILIES = [
     ("f16_tn", (600, 1100, 520), (0, 0, 0), (1, 256, 1), "_pair_256x256"),   # CTA pair, whole tiles
     ("tf32", (2500, 4500, 1000), (0, 0, 0), (5, 256, 2), "_sk_"),         # wide pair, stream-K tail
     ("f16_tn", (2304, 2304, 512), (0, 0, 0), (1, 256, 2), "_sk_"),        # pair, stream-K tail
-    ("bf16_nn", (300, 700, 200), (0, 0, 0), (2, 128, 1), "_128x128"),     # single-CTA kernel
+    ("bf16_nn", (300, 704, 200), (0, 0, 0), (2, 128, 1), "_128x128"),     # single-CTA kernel
     ("f16_tn", (100, 1000, 2048), (0, 0, 0), None, "_splitk"),            # split-K in clusters (DSMEM)
     ("tf32", (300, 520, 130), (1, 2, 0), None, "_cpasync"),               # cp.async producer
     ("f16_nn", (300, 520, 130), (1, 2, 0), None, "_ldst"),                # register-path producer
