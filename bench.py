@@ -285,8 +285,10 @@ def run_ours(args):
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         ev = {p: [{k: torch.cuda.Event() for k in ("in", "gemm", "out")} for _ in range(2)] for p in paths_run}
 
+        # the e2e leg runs as many steps as the device-timed leg (at most 40)
+        e2e_steps = max(1, min(args.steps, 40))
         gemm_ev = [{p: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                    for p in paths_run} for _ in range(max(1, min(args.steps, 10)))]
+                    for p in paths_run} for _ in range(e2e_steps)]
 
         def e2e_step(i, timed=False):
             b = i % 2
@@ -313,7 +315,6 @@ def run_ours(args):
                     hosts_c[p].copy_(Cd, non_blocking=True)
                 ev[p][b]["out"].record(s_out)
 
-        e2e_steps = max(1, min(args.steps, 10))
         e2e_step(0)
         e2e_step(1)
         torch.cuda.synchronize()

@@ -1,7 +1,8 @@
 """GEMM calls captured in a CUDA graph and replayed.
 
 A sequence of calls -- the CTA-pair kernel (FP16 TN, TF32), the FP32 SIMT
-kernel, split-K in clusters, the single-CTA kernel and the workspace path --
+kernels (split-K in clusters and the TMA-fed one), split-K in clusters on
+the tensor cores, the single-CTA kernel and the workspace path --
 is captured once on a side stream after one eager warm-up call of each (the
 library's per-device caches are filled outside the capture), then replayed.
 Every replay must give exactly the eager results: the kernels are
@@ -19,7 +20,7 @@ def _problems():
     out = []
     for path, (M, N, K), seed in (("f16_tn", (1024, 2048, 512), 1), ("tf32", (768, 1536, 1000), 2),
                                   ("f32", (300, 520, 1000), 3), ("f16_tn", (100, 1000, 2048), 4),
-                                  ("bf16_nn", (129, 260, 72), 5)):
+                                  ("bf16_nn", (129, 260, 72), 5), ("f32", (2176, 2304, 96), 7)):
         A, B, C = parity.host_operands(path, M, N, K, seed=seed)
         out.append((path, A.cuda(), B.cuda(), C.cuda()))
     return out
