@@ -484,8 +484,11 @@ __device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_
 //                   reads for N-major 32-bit operands).
 // The swizzle pattern is anchored at 1024-byte boundaries, so every tile base
 // handed to this must be 1024-byte aligned (base offset 0).
+//   kSw64      (4): 64-byte swizzle of 16-byte chunks, 8 rows x 64 B atoms
+//                   (the pattern repeats every 512 bytes).
 constexpr uint32_t kSw128 = 2;
 constexpr uint32_t kSw128A32 = 1;
+constexpr uint32_t kSw64 = 4;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint32_t layout)

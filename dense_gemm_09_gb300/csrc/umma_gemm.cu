@@ -1158,6 +1158,7 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
 // at ~97 % of its peak when the operands are already in shared memory.
 
 constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_MAX_STAGES = 12;                // the finer ring (see PairShape)
 constexpr int PAIR_BM = 2 * BM;                    // rows per pair tile
 constexpr int PAIR_HALF_BYTES = 128 * ROW_BYTES;   // 16 KB: 128 rows of A or of B
 constexpr int PAIR_STAGE_BYTES = 2 * PAIR_HALF_BYTES;
@@ -1172,11 +1173,11 @@ constexpr int pair_threads()
 }
 constexpr int PAIR_MMA_WARP = 1;
 constexpr int PAIR_WAITER_WARP = 6;
-constexpr uint32_t PAIR_HANDOFF_THREADS = 64;  // warps 1 and 6 on named barriers 1..PAIR_STAGES
+constexpr uint32_t PAIR_HANDOFF_THREADS = 64;  // warps 1 and 6 on named barriers 1..stages
 
 struct PairCtrl {
-    uint64_t full[PAIR_STAGES];   // even CTA: both halves of the stage landed
-    uint64_t empty[PAIR_STAGES];  // the pair's MMAs have read this stage
+    uint64_t full[PAIR_MAX_STAGES];   // even CTA: both halves of the stage landed
+    uint64_t empty[PAIR_MAX_STAGES];  // the pair's MMAs have read this stage
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t acc_ready;  // stream-K: every epilogue warp has loaded its part of a partial
@@ -1206,12 +1207,24 @@ __device__ __forceinline__ void pair_tile(int64_t t, const Params &p, int64_t &m
 // CTA loads 16 KB of A and 32 KB of B per stage for twice the MMA work --
 // a quarter fewer bytes per flop into every SM -- at the price of a single
 // accumulator, whose drain the next tile's MMAs wait for.
-template <int kWide>
+//
+// kRowB is the K depth of a stage in bytes per row: 128 (one 128-byte
+// swizzled row: 64 f16 / 32 f32 elements), or 64 -- the finer ring of the
+// K-major 16-bit kinds: rows of 32 elements under the 64-byte swizzle, so a
+// stage is half as large, the same 192 KB hold twice as many, and the MMAs
+// release their stage after two instructions instead of four.
+template <int kWide, int kRowB = ROW_BYTES>
 struct PairShape {
-    static constexpr int kStageBytes = PAIR_HALF_BYTES * (1 + kWide);  // A half + kWide B halves
-    static constexpr int kStages = PAIR_STAGES * PAIR_STAGE_BYTES / kStageBytes;  // 6 or 4
-    static constexpr int kAccs = 2 / kWide;                                 // TMEM accumulators
+    static constexpr int kHalfBytes = 128 * kRowB;                      // 128 rows of A or of B
+    static constexpr int kStageBytes = kHalfBytes * (1 + kWide);        // A half + kWide B halves
+    static constexpr int kStages = PAIR_STAGES * PAIR_STAGE_BYTES / kStageBytes;  // 6 / 4, or 12 / 8
+    static constexpr int kAccs = 2 / kWide;                             // TMEM accumulators
     static constexpr int kAccCols = BN * kWide;
+    static constexpr uint32_t kSbo = 8u * kRowB;                        // bytes between 8-row groups
+    static constexpr uint32_t kLayout = kRowB == ROW_BYTES ? ptx::kSw128 : ptx::kSw64;
+    static_assert(kRowB == ROW_BYTES || kRowB == 64, "stages of 128 or 64 bytes of K per row");
+    static_assert(kStages <= PAIR_MAX_STAGES, "barriers for every stage");
+    static_assert(kStageBytes % 1024 == 0, "stages start on the swizzle pattern's period");
 };
 
 // ---- stream-K tail
@@ -1407,13 +1420,14 @@ __device__ __forceinline__ bool sk_init(const Params &p, uint32_t taddr, int64_t
     return true;
 }
 
-template <int kKind, int kWide>
+template <int kKind, int kWide, int kRowB>
 __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
                                               const Params &p, uint32_t smem_base, PairCtrl *ctrl,
                                               uint32_t rank, WaitCtl *wc)
 {
     using T = Traits<kKind>;
-    using S = PairShape<kWide>;
+    using S = PairShape<kWide, kRowB>;
+    constexpr int kStageK = kRowB / T::kElem;  // K elements per stage
     const int64_t cluster = blockIdx.x / 2, clusters = gridDim.x / 2;
     const uint32_t half = rank & 1u;
     uint32_t stage = 0, phase = 0;
@@ -1433,11 +1447,11 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
             const uint32_t full = ptx::mapa(full_local, 0);  // the pair leader's barrier
             if (half == 0) ptx::mbar_arrive_expect_tx(full_local, 2 * S::kStageBytes);
             const uint32_t sa = smem_base + stage * S::kStageBytes;
-            const int32_t kc = static_cast<int32_t>(kb * T::BK);
+            const int32_t kc = static_cast<int32_t>(kb * kStageK);
             ptx::tma_load_2d_pair(sa, tmap_a, full, kc, static_cast<int32_t>(m0 + half * 128));
 #pragma unroll
             for (int w = 0; w < kWide; ++w) {
-                const uint32_t sb = sa + (1 + w) * PAIR_HALF_BYTES;
+                const uint32_t sb = sa + (1 + w) * S::kHalfBytes;
                 const int64_t nb = n0 + w * BN + half * 128;  // this CTA's half of B, MMA w
                 if constexpr (!T::kBNMajor) {
                     ptx::tma_load_2d_pair(sb, tmap_b, full, kc, static_cast<int32_t>(nb));
@@ -1474,10 +1488,10 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
 // named barrier 1 + stage.  The barrier's OR-reduction carries the abort flag
 // both ways, so each side runs through the same number of hand-offs and
 // neither can be left waiting on the other after a time-out.
-template <int kKind, int kWide>
+template <int kKind, int kWide, int kRowB>
 __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int lane, WaitCtl *wc)
 {
-    using S = PairShape<kWide>;
+    using S = PairShape<kWide, kRowB>;
     const int64_t cluster = blockIdx.x / 2, clusters = gridDim.x / 2;
     uint32_t stage = 0, phase = 0;
     bool abort = false;
@@ -1503,12 +1517,13 @@ __device__ __forceinline__ void pair_waiter(const Params &p, PairCtrl *ctrl, int
 // takes the hand-off from the waiter, issues the stage's MMAs and commits the
 // stage's release to the "empty" barriers of both CTAs; per tile it waits
 // for a free accumulator and commits "tmem_full" to both CTAs.
-template <int kKind, int kWide>
+template <int kKind, int kWide, int kRowB>
 __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, PairCtrl *ctrl,
                                          uint32_t tmem_base, uint32_t rank, int lane, WaitCtl *wc)
 {
     using T = Traits<kKind>;
-    using S = PairShape<kWide>;
+    using S = PairShape<kWide, kRowB>;
+    constexpr int kStageK = kRowB / T::kElem;  // K elements per stage
     constexpr uint16_t kBoth = 0x3;  // the two CTAs of the pair
     const int64_t cluster = blockIdx.x / 2, clusters = gridDim.x / 2;
     uint32_t stage = 0, acc = 0, acc_phase = 0, ready_phase = 0;
@@ -1537,14 +1552,16 @@ __device__ __forceinline__ void pair_mma(const Params &p, uint32_t smem_base, Pa
                 if (lane == 0) {
                     const uint32_t sa = smem_base + stage * S::kStageBytes;
 #pragma unroll
-                    for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
-                        const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
+                    for (int k = 0; k < kStageK / T::UMMA_K; ++k) {
+                        // K-major: advance 32 bytes along the swizzled row; 8-row
+                        // groups are 8 rows of kRowB bytes apart
+                        const uint64_t da = ptx::smem_desc(sa + k * 32, 16, S::kSbo, S::kLayout);
 #pragma unroll
                         for (int w = 0; w < kWide; ++w) {
-                            const uint32_t sb = sa + (1 + w) * PAIR_HALF_BYTES;
+                            const uint32_t sb = sa + (1 + w) * S::kHalfBytes;
                             uint64_t db;
                             if constexpr (!T::kBNMajor)
-                                db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
+                                db = ptx::smem_desc(sb + k * 32, 16, S::kSbo, S::kLayout);
                             else
                                 db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
                             ptx::umma_pair<kKind>(d_tmem + w * BN, da, db, pair_idesc<kKind>(),
@@ -1639,12 +1656,13 @@ __device__ __forceinline__ void pair_epilogue(const Params &p, const CUtensorMap
     if (lane == 0) ptx::bulk_wait<0>();  // stores done before the CTA leaves
 }
 
-template <int kKind, int kWide>
+template <int kKind, int kWide, int kRowB = ROW_BYTES>
 __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     umma_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, const Params p)
 {
+    static_assert(kRowB == ROW_BYTES || !Traits<kKind>::kBNMajor, "the finer ring is for K-major operands");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1654,7 +1672,7 @@ __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     const bool leader = (rank & 1u) == 0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < PAIR_STAGES; ++s) {
+        for (int s = 0; s < PAIR_MAX_STAGES; ++s) {
             ptx::mbar_init(ptx::smem_addr(&ctrl->full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), 1);
         }
@@ -1686,11 +1704,11 @@ __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     const uint32_t smem_base = ptx::smem_addr(smem);
 
     if (warp == 0) {
-        if (lane == 0) pair_producer<kKind, kWide>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
+        if (lane == 0) pair_producer<kKind, kWide, kRowB>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
     } else if (warp == PAIR_MMA_WARP) {
-        if (leader) pair_mma<kKind, kWide>(p, smem_base, ctrl, tmem_base, rank, lane, wc);
+        if (leader) pair_mma<kKind, kWide, kRowB>(p, smem_base, ctrl, tmem_base, rank, lane, wc);
     } else if (warp == PAIR_WAITER_WARP) {
-        if (leader) pair_waiter<kKind, kWide>(p, ctrl, lane, wc);
+        if (leader) pair_waiter<kKind, kWide, kRowB>(p, ctrl, lane, wc);
     } else {
         pair_epilogue<kKind, kWide>(p, &tmap_c, ctrl, tmem_base, smem_base + PAIR_STAGES * PAIR_STAGE_BYTES,
                                      rank, warp, lane, wc);
@@ -1771,7 +1789,7 @@ bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
 
 // Co-resident clusters of the pair kernel (clusters of 2 CTAs) on the
 // current device (0 if the kernel cannot run), cached per device and kind.
-template <int kKind, int kWide = 1>
+template <int kKind, int kWide = 1, int kRowB = ROW_BYTES>
 int pair_clusters()
 {
     constexpr int kMaxDevices = 64;
@@ -1781,7 +1799,7 @@ int pair_clusters()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     std::call_once(once[dev], [dev] {
         int n = 0;
-        if (cudaFuncSetAttribute(umma_pair_kernel<kKind, kWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(umma_pair_kernel<kKind, kWide, kRowB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PAIR_SMEM_BYTES) == cudaSuccess) {
             int sms = 0;
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1796,7 +1814,7 @@ int pair_clusters()
             cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, umma_pair_kernel<kKind, kWide>, &cfg) != cudaSuccess) n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, umma_pair_kernel<kKind, kWide, kRowB>, &cfg) != cudaSuccess) n = 0;
         }
         cudaGetLastError();  // a failed query leaves no sticky error behind
         cached[dev] = n;
@@ -1895,12 +1913,12 @@ int64_t stream_k_tiles(int64_t tiles, int64_t pairs, int64_t num_kb, double kb_u
 // p.tiles_m / p.tiles_n count 256-row bands and tile columns (p.bn columns
 // each).  sk_mode: kSkAuto / kSkOff / kSkOn.
 // *sk tells whether the launch used stream-K.
-template <int kKind, int kWide = 1>
+template <int kKind, int kWide = 1, int kRowB = ROW_BYTES>
 bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, Params p,
                  cudaStream_t stream, int sk_mode = kSkOff, bool *sk = nullptr)
 {
     if (sk) *sk = false;
-    const int clusters = pair_clusters<kKind, kWide>();
+    const int clusters = pair_clusters<kKind, kWide, kRowB>();
     if (clusters <= 0) return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
     const int64_t n = tiles < clusters ? tiles : clusters;
@@ -1916,7 +1934,8 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    p.sk_tiles = stream_k_tiles(tiles, n, p.num_kb, kSkKbUs * kWide, sk_mode);
+    // (a K block of the finer ring is half as deep: half the time)
+    p.sk_tiles = stream_k_tiles(tiles, n, p.num_kb, kSkKbUs * kWide * kRowB / ROW_BYTES, sk_mode);
     int dev = -1;
     SkWorkspace *w = nullptr;
     if (p.sk_tiles > 0 && !stream_capturing(stream) && cudaGetDevice(&dev) == cudaSuccess)
@@ -1931,7 +1950,7 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
             p.sk_work = w->work;
             p.sk_flags = w->flags;
             p.sk_gen = ++w->gen;
-            if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide>, ma, mb, mc, p) != cudaSuccess) {
+            if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide, kRowB>, ma, mb, mc, p) != cudaSuccess) {
                 cudaGetLastError();
                 return false;
             }
@@ -1942,7 +1961,7 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
         }
     }
     p.sk_tiles = 0;
-    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide>, ma, mb, mc, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide, kRowB>, ma, mb, mc, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -2037,7 +2056,10 @@ int cluster_capacity(int size)
 // persistent single-CTA kernel (128 x bn tiles) or split-K over S CTAs of a
 // cluster (128 x bn tiles).
 // (4 is unused: it once named a two-pair cluster variant, since removed.)
-enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3, kVariantWide = 5 };
+// 6 and 7: the pair kernels with the finer ring (32-deep K stages of the
+// K-major 16-bit kinds, see PairShape).
+enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3, kVariantWide = 5,
+       kVariantPairFine = 6, kVariantWideFine = 7 };
 struct UmmaConfig {
     int variant;
     int bn;
@@ -2176,7 +2198,7 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorM
 template <int kKind>
 const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = false)
 {
-    static std::string names[6 + 9 * 9];  // [2 + 9 * 9] unused
+    static std::string names[10 + 9 * 9];  // [2 + 9 * 9] unused
     static std::once_flag once;
     std::call_once(once, [] {
         using T = Traits<kKind>;
@@ -2188,6 +2210,11 @@ const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = fals
         names[3 + 9 * 9] = base + "_pair_256x512x" + bk + "_tma";
         names[4 + 9 * 9] = base + "_pair_256x256x" + bk + "_sk_tma";
         names[5 + 9 * 9] = base + "_pair_256x512x" + bk + "_sk_tma";
+        const std::string bkf = std::to_string(64 / T::kElem);  // the finer ring's K per stage
+        names[6 + 9 * 9] = base + "_pair_256x256x" + bkf + "_tma";
+        names[7 + 9 * 9] = base + "_pair_256x256x" + bkf + "_sk_tma";
+        names[8 + 9 * 9] = base + "_pair_256x512x" + bkf + "_tma";
+        names[9 + 9 * 9] = base + "_pair_256x512x" + bkf + "_sk_tma";
         names[1] = base + "_128x256x" + bk + (kKind == kTF32 ? "_cpasync" : "_ldst");
         for (int w = 1; w <= 8; ++w) {
             const std::string tile = "128x" + std::to_string(32 * w) + "x" + bk;
@@ -2198,6 +2225,8 @@ const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = fals
     });
     if (variant == kVariantPair) return names[sk ? 4 + 9 * 9 : 0].c_str();
     if (variant == kVariantWide) return names[sk ? 5 + 9 * 9 : 3 + 9 * 9].c_str();
+    if (variant == kVariantPairFine) return names[sk ? 7 + 9 * 9 : 6 + 9 * 9].c_str();
+    if (variant == kVariantWideFine) return names[sk ? 9 + 9 * 9 : 8 + 9 * 9].c_str();
     if (variant == kVariantAuto) return names[1].c_str();  // the non-TMA kernel
     const int w = bn / 32, S = variant == kVariantSplit ? split : 1;
     return names[2 + w * 9 + S].c_str();
@@ -2218,11 +2247,16 @@ void set_ring(Params &p, bool split)
 // pair kernel (null if B cannot be described); make_b(bn, map) builds B's map
 // for 128 x bn tiles.
 template <int kKind, typename MakeB>
-const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *mb_pair, int pair3d, MakeB make_b, const CUtensorMap &mc,
+const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *mb_pair,
+                         const CUtensorMap *ma_fine, const CUtensorMap *mb_fine, int pair3d, MakeB make_b, const CUtensorMap &mc,
                          cudaStream_t stream, const DeviceInfo &dev)
 {
     UmmaConfig cfg = t_tune;
     t_tune = UmmaConfig{kVariantAuto, BN, 1};
+    // the finer ring needs its own tensor maps (K-major 16-bit operands);
+    // without them a request for it takes the ordinary ring
+    if (cfg.variant == kVariantPairFine && !(ma_fine && mb_fine)) cfg.variant = kVariantPair;
+    if (cfg.variant == kVariantWideFine && !(ma_fine && mb_fine)) cfg.variant = kVariantWide;
     if (((cfg.variant == kVariantPair || cfg.variant == kVariantWide) && !mb_pair) || cfg.bn % bn_step<kKind>() != 0)
         cfg.variant = kVariantAuto;
     // every rank of a split needs at least one K block
@@ -2232,6 +2266,25 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
     if (cfg.variant == kVariantAuto)
         cfg = choose_config<kKind>(p0, dev.sm_count, mb_pair != nullptr);
     Params p = p0;
+    if constexpr (!Traits<kKind>::kBNMajor) {
+        if (cfg.variant == kVariantPairFine || cfg.variant == kVariantWideFine) {
+            const bool wide = cfg.variant == kVariantWideFine;
+            Params f = p;
+            f.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
+            f.b3d = 0;
+            f.num_kb = (p.K + 64 / Traits<kKind>::kElem - 1) / (64 / Traits<kKind>::kElem);  // 32-deep K blocks
+            if (wide) {
+                f.bn = 2 * BN;  // 256 x 512 pair tiles
+                f.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);
+                if (f.bn % box_cols<kKind>() != 0) f.tma_store = 0;
+            }
+            bool sk = false;
+            const bool ok = wide ? launch_pair<kKind, 2, 64>(*ma_fine, *mb_fine, mc, f, stream, cfg.split, &sk)
+                                 : launch_pair<kKind, 1, 64>(*ma_fine, *mb_fine, mc, f, stream, cfg.split, &sk);
+            if (ok) return variant_name<kKind>(cfg.variant, BN, 1, sk);
+            cfg.variant = wide ? kVariantWide : kVariantPair;
+        }
+    }
     if (cfg.variant == kVariantPair || cfg.variant == kVariantWide) {
         p.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
         p.b3d = pair3d;
@@ -2328,7 +2381,14 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
         int probe3d = 0, pair3d = 0;
         if (make_b(BN, &probe, &probe3d)) {
             const bool ok_pair = make_b(128, &mbp, &pair3d);
-            return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, pair3d, make_b, mc, stream, dev);
+            // the finer ring (K-major 16-bit kinds): 32-element boxes under the 64-byte swizzle
+            CUtensorMap maf{}, mbf{};
+            bool ok_fine = false;
+            if constexpr (!T::kBNMajor && T::kElem == 2)
+                ok_fine = make_map(&maf, dt, A, K, M, lda * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) &&
+                          make_map(&mbf, dt, B, K, N, ldb * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+            return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, ok_fine ? &maf : nullptr,
+                                       ok_fine ? &mbf : nullptr, pair3d, make_b, mc, stream, dev);
         }
     }
     t_tune = UmmaConfig{kVariantAuto, BN, 1};
@@ -2360,11 +2420,12 @@ const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, 
 
 int umma_tune_next(int variant, int bn, int split)
 {
-    if (variant < kVariantAuto || variant > kVariantWide || variant == 4) return DGEMM_ERR_INVALID_ARG;
+    if (variant < kVariantAuto || variant > kVariantWideFine || variant == 4) return DGEMM_ERR_INVALID_ARG;
     if ((variant == kVariantSingle || variant == kVariantSplit) && (bn < 32 || bn > BN || bn % 32 != 0))
         return DGEMM_ERR_INVALID_ARG;
     if (variant == kVariantSplit && (split < 2 || split > 8)) return DGEMM_ERR_INVALID_ARG;
-    const bool paired = variant == kVariantPair || variant == kVariantWide;
+    const bool paired = variant == kVariantPair || variant == kVariantWide || variant == kVariantPairFine ||
+                        variant == kVariantWideFine;
     if (paired && (split < kSkAuto || split > kSkOn)) return DGEMM_ERR_INVALID_ARG;
     const bool sized = variant == kVariantSingle || variant == kVariantSplit;
     t_tune = UmmaConfig{variant, sized ? bn : BN, variant == kVariantSplit || paired ? split : 1};

@@ -367,12 +367,16 @@ int dgemm_test_choose_config(int kind, int64_t M, int64_t N, int64_t K, int sm_c
  *           3: split-K, `split` CTAs of a cluster per 128 x bn tile;
  *           4: not a variant (rejected with DGEMM_ERR_INVALID_ARG);
  *           5: CTA pair, 256 x 512 output tiles (one 512-column
- *              accumulator per CTA).
+ *              accumulator per CTA);
+ *           6, 7: as 1 and 5 with the finer stage ring of the K-major
+ *              16-bit calls (gemm_f16_tn, gemm_bf16_tn): 32-deep K stages
+ *              under the 64-byte swizzle, twice as many in the same
+ *              shared memory; other calls take 1 or 5 instead.
  *   bn:    tile width for variants 2 and 3: 32..256 in steps of 32; the
  *          NN 16-bit calls need a multiple of 64.  Ignored otherwise.
  *   split: 2..8 for variant 3 (lowered to the number of K blocks when K is
- *          shorter, so that every CTA has work); for variants 1 and 5 the
- *          stream-K mode: 0 automatic, 1 whole tiles only, 2 cut the first
+ *          shorter, so that every CTA has work); for variants 1, 5, 6 and 7
+ *          the stream-K mode: 0 automatic, 1 whole tiles only, 2 cut the first
  *          P + (T mod P) of T tiles whenever they outnumber the P pairs;
  *          ignored otherwise.
  * Returns DGEMM_ERR_INVALID_ARG (and records nothing) for values outside

@@ -51,6 +51,35 @@ def test_stream_k_equals_round_robin_bitwise(path, M, N, K, wide):
     assert torch.equal(whole, cut)
 
 
+@pytest.mark.parametrize("path", ["f16_tn", "bf16_tn"])
+@pytest.mark.parametrize("wide", [True, False], ids=["256x512", "256x256"])
+def test_finer_ring_matches_oracle_and_coarse_ring(path, wide):
+    """The finer stage ring (32-deep K stages under the 64-byte swizzle) runs
+    the same MMAs in the same K order as the ordinary ring: results agree
+    bit for bit, whole tiles and stream-K alike, and with the oracle."""
+    import dense_gemm_09_gb300 as dg
+    M, N, K = (2500, 4500, 1000) if wide else (2304, 2304, 1000)
+    A, B, C = parity.host_operands(path, M, N, K, seed=M + K)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    coarse = dg.TUNE_PAIR_WIDE if wide else dg.TUNE_PAIR
+    fine = dg.TUNE_PAIR_WIDE_FINE if wide else dg.TUNE_PAIR_FINE
+    want, _ = _run(path, dA, dB, dC, 0.75, 0.5, coarse, dg.SK_OFF)
+    for sk in (dg.SK_OFF, dg.SK_ON):
+        got, name = _run(path, dA, dB, dC, 0.75, 0.5, fine, sk)
+        assert ("x32_sk_tma" if sk == dg.SK_ON else "x32_tma") in name, name
+        assert dg.device_status() == dg.OK
+        assert torch.equal(got, want)
+    assert parity.worst_ratio(path, got.cpu(), A, B, C, 0.75, 0.5) <= 1.0
+
+
+def test_finer_ring_request_falls_back_for_n_major_kinds():
+    import dense_gemm_09_gb300 as dg
+    A, B, C = parity.host_operands("tf32", 600, 1100, 520, seed=3)
+    got, name = _run("tf32", A.cuda(), B.cuda(), C.cuda(), 1.0, 0.0, dg.TUNE_PAIR_FINE, dg.SK_OFF)
+    assert "_pair_256x256x32_tma" in name, name  # the ordinary ring (TF32's stages are 32 deep already)
+    assert parity.worst_ratio("tf32", got.cpu(), A, B, C, 1.0, 0.0) <= 1.0
+
+
 @pytest.mark.parametrize("path", ["f16_tn", "tf32"])
 def test_stream_k_matches_oracle(path):
     import dense_gemm_09_gb300 as dg
