@@ -260,16 +260,28 @@ extern "C" int gemm_f32_ws(int64_t M, int64_t N, int64_t K, float alpha, const f
     DeviceInfo dev;
     if ((st = check_device(dev)) != DGEMM_OK) return st;
     if (K == 0 || alpha == 0.f) return finish(launch_scale_f32(M, N, beta, C, ldc, stream));
-    // only B is copied: the SIMT kernel loads A element by element whatever
-    // its alignment, and B in 16-byte pieces when its rows allow
+    // B is copied when its rows rule out 16-byte loads.  A is copied too when
+    // the problem runs as one plain launch (at least a wave of tiles): with
+    // both operands TMA-describable the TMA-fed kernel runs, and the copy
+    // (one pass over A at HBM speed) is small against the GEMM.  Smaller
+    // problems (split-K) load A element by element, so A stays in place.
     const Tf32Repack r = plan_tf32_repack(M, N, K, A, lda, B, ldb);
     if (r.bytes < 0) return DGEMM_ERR_INVALID_ARG;
-    if (r.b) {
+    const bool copy_a = r.a && sgemm_simt_plain_launch(M, N, K, dev);
+    if (r.b || copy_a) {
         if (!workspace || workspace_bytes < r.bytes || !aligned16(workspace)) return DGEMM_ERR_INVALID_ARG;
-        float *wb = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + r.off_b);
-        if (!launch_repack_f32(B, K, N, ldb, wb, r.ldb, stream, dev)) return DGEMM_ERR_LAUNCH;
-        B = wb;
-        ldb = r.ldb;
+        if (copy_a) {
+            float *wa = static_cast<float *>(workspace);
+            if (!launch_repack_f32(A, M, K, lda, wa, r.lda, stream, dev)) return DGEMM_ERR_LAUNCH;
+            A = wa;
+            lda = r.lda;
+        }
+        if (r.b) {
+            float *wb = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + r.off_b);
+            if (!launch_repack_f32(B, K, N, ldb, wb, r.ldb, stream, dev)) return DGEMM_ERR_LAUNCH;
+            B = wb;
+            ldb = r.ldb;
+        }
     }
     return finish(launch_sgemm_simt(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, dev));
 }

@@ -38,6 +38,11 @@ const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, cons
                               int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                               int64_t ldc, cudaStream_t stream, const DeviceInfo &dev);
 
+// Whether the FP32 SIMT path would run this problem as one plain launch (at
+// least a wave of tiles, or K too short to split) -- the case in which
+// TMA-describable operands take the TMA-fed kernel.
+bool sgemm_simt_plain_launch(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev);
+
 // FP32 SIMT path fed by TMA (A and B with 16-byte aligned bases and row
 // pitches; the caller checks that).  nullptr if it cannot be used for this
 // call (sizes beyond TMA's coordinates, a refused tensor map), in which case

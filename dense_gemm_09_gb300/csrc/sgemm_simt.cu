@@ -483,6 +483,16 @@ const char *simt_name(bool vec, const SimtPlan &pl)
 
 }  // namespace
 
+bool sgemm_simt_plain_launch(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
+{
+    int device = 0;
+    cudaGetDevice(&device);
+    const SimtOccupancy &occ = occupancy<true>(device);
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    return plan_simt(tiles, (K + BK - 1) / BK, static_cast<int64_t>(occ.blocks_per_sm) * dev.sm_count, occ).mode ==
+           kPlain;
+}
+
 const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                               int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                               int64_t ldc, cudaStream_t stream, const DeviceInfo &dev)
@@ -492,16 +502,9 @@ const char *launch_sgemm_simt(int64_t M, int64_t N, int64_t K, float alpha, cons
     const bool vec_c = aligned16(C) && (ldc % 4 == 0);
     // Problems of at least a wave of tiles whose A and B TMA can describe
     // take the TMA-fed kernel (sgemm_tma.cu).
-    if (vec_b && aligned16(A) && (lda % 4 == 0)) {
-        int device = 0;
-        cudaGetDevice(&device);
-        const SimtOccupancy &occ = occupancy<true>(device);
-        const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-        if (plan_simt(tiles, (K + BK - 1) / BK, static_cast<int64_t>(occ.blocks_per_sm) * dev.sm_count, occ).mode ==
-            kPlain) {
-            if (const char *name = launch_sgemm_tma(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
-                return name;
-        }
+    if (vec_b && aligned16(A) && (lda % 4 == 0) && sgemm_simt_plain_launch(M, N, K, dev)) {
+        if (const char *name = launch_sgemm_tma(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
+            return name;
     }
     SimtPlan pl{kPlain, 1};
     const bool ok =

@@ -159,13 +159,15 @@ int64_t gemm_tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, const float *
 
 /*
  * gemm_f32_ws -- gemm_f32 with the workspace of gemm_tf32_ws (same layout,
- * same size: gemm_tf32_workspace_bytes, of which it uses only B's part).
- * When B's base or row pitch is not a 16-byte multiple (e.g. ldb = N = 8193),
- * B is first copied bit for bit into the workspace with a padded pitch, so
- * that the SIMT kernel loads it in 16-byte pieces instead of 4-byte ones; A
- * is loaded element by element in either case and is not copied.  Results
- * are the same as gemm_f32 on the same values.  Workspace rules and errors
- * as gemm_tf32_ws; the call allocates nothing.
+ * same size: gemm_tf32_workspace_bytes).  When B's base or row pitch is not
+ * a 16-byte multiple (e.g. ldb = N = 8193), B is first copied bit for bit
+ * into the workspace with a padded pitch, so that the SIMT kernels load it
+ * in 16-byte pieces (or by TMA) instead of 4-byte ones.  When A's base or
+ * pitch is not a 16-byte multiple either and the problem has at least a
+ * wave of output tiles, A is copied too, so that the TMA-fed kernel runs;
+ * smaller problems (split-K) load A element by element and leave it in
+ * place.  Results are the same as gemm_f32 on the same values.  Workspace
+ * rules and errors as gemm_tf32_ws; the call allocates nothing.
  * Source: the operation of gemm_f32 ("SGEMM CUDA代码学习", "第 5 步":
  * 16-byte asynchronous copies need 16-byte aligned addresses).
  */

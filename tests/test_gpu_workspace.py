@@ -127,12 +127,16 @@ def test_ws_ragged_workload_full_size():
     assert parity.sampled_check("tf32", dC, A, B, C, w.alpha, w.beta) <= 1.0
 
 
-# gemm_f32_ws: the SIMT path with the same workspace; only B is copied.
+# gemm_f32_ws: the SIMT path with the same workspace.  B is copied when its
+# rows rule out 16-byte loads; A is copied too when the problem has at least
+# a wave of tiles (then the TMA-fed kernel runs), and otherwise stays in place.
 F32_CASES = [
     (129, 257, 301, (0, 0), (0, 0)),      # odd N: B's pitch off 16 bytes
     (300, 520, 1000, (0, 3), (0, 0)),     # B pitch 523
     (300, 520, 1000, (0, 0), (0, 2)),     # B base off 16 bytes
     (1000, 1100, 513, (2, 2), (3, 1)),
+    (2100, 2500, 301, (0, 0), (0, 0)),    # a wave of tiles: A (pitch 301) and B (2500 ok) -> A copied
+    (2049, 2561, 300, (1, 0), (0, 0)),    # a wave of tiles: A pitch 301, B pitch 2561: both copied
 ]
 
 
@@ -147,8 +151,13 @@ def test_f32_ws_matches_oracle_and_plain_call(M, N, K, pad, offset):
     got = C.cuda()
     dg.gemm_f32_ws(dA, dB, got, 1.5, -0.25, workspace=ws)
     torch.cuda.synchronize()
-    # B now loads in 16-byte pieces (or by TMA, when A allows it too)
-    assert not dg.last_kernel().endswith("cpasync4"), dg.last_kernel()
+    # B now loads in 16-byte pieces, or both operands by TMA when the problem
+    # has at least a wave of tiles
+    big = ((M + 127) // 128) * ((N + 127) // 128) >= 304
+    if big:
+        assert dg.last_kernel().startswith("sgemm_simt_tma_"), dg.last_kernel()
+    else:
+        assert not dg.last_kernel().endswith("cpasync4"), dg.last_kernel()
     assert parity.worst_ratio("f32", got.cpu(), A, B, C, 1.5, -0.25) <= 1.0
     # the same FP32 FMAs in the same order as the plain call on the same values
     want = C.cuda()
