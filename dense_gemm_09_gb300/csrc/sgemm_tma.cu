@@ -36,6 +36,7 @@
 //     DGEMM_ERR_TIMEOUT in this file's device status word, the CTA stops,
 //     and one thread waits (again bounded) for the copies it issued before
 //     the CTA leaves.
+#include <climits>
 #include <cstdint>
 #include <mutex>
 
@@ -352,6 +353,8 @@ const char *launch_sgemm_tma(int64_t M, int64_t N, int64_t K, float alpha, const
     // TMA coordinates are 32-bit; the caller has checked alignment
     constexpr int64_t kCoordMax = (int64_t(1) << 31) - 256;
     if (M > kCoordMax || N > kCoordMax || K > kCoordMax) return nullptr;
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + Cfg::BN - 1) / Cfg::BN);
+    if (tiles > INT32_MAX) return nullptr;  // (a C of 2^45 elements: no GPU holds one)
     CUtensorMap ma, mb;
     if (!encode_tiled_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, static_cast<uint64_t>(K),
                          static_cast<uint64_t>(M), static_cast<uint64_t>(lda) * 4, BK, BM,
@@ -375,7 +378,6 @@ const char *launch_sgemm_tma(int64_t M, int64_t N, int64_t K, float alpha, const
     p.wait_limit_ns = stall ? stall : kWaitLimitNs;
     const int64_t shrink = take_shrink_bounds();
     p.m_checked = shrink < M ? M - shrink : 0;
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + Cfg::BN - 1) / Cfg::BN);
     kKernel<<<static_cast<unsigned>(tiles), Cfg::THREADS, kSmemBytes, stream>>>(ma, mb, p);
     return "sgemm_simt_tma_128x128x32_ffma2";
 }

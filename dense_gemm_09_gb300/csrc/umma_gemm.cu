@@ -2381,12 +2381,14 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
         int probe3d = 0, pair3d = 0;
         if (make_b(BN, &probe, &probe3d)) {
             const bool ok_pair = make_b(128, &mbp, &pair3d);
-            // the finer ring (K-major 16-bit kinds): 32-element boxes under the 64-byte swizzle
+            // the finer ring (K-major 16-bit kinds, only on request through the
+            // tuning hook): 32-element boxes under the 64-byte swizzle
             CUtensorMap maf{}, mbf{};
             bool ok_fine = false;
             if constexpr (!T::kBNMajor && T::kElem == 2)
-                ok_fine = make_map(&maf, dt, A, K, M, lda * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) &&
-                          make_map(&mbf, dt, B, K, N, ldb * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+                if (t_tune.variant == kVariantPairFine || t_tune.variant == kVariantWideFine)
+                    ok_fine = make_map(&maf, dt, A, K, M, lda * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) &&
+                              make_map(&mbf, dt, B, K, N, ldb * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
             return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, ok_fine ? &maf : nullptr,
                                        ok_fine ? &mbf : nullptr, pair3d, make_b, mc, stream, dev);
         }
