@@ -40,6 +40,7 @@
 // abort flag that the other roles also poll, waits (again bounded) for its
 // own copies and MMAs in flight, and the CTA releases its TMEM and exits.
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <mutex>
 #include <string>
@@ -208,8 +209,12 @@ struct Params {
     int stages, stage_bytes;
     // CTA-pair kernel with N-major B: the stage's B half comes as one 3-D box
     // (column group of 128 bytes x BK rows x 128 / kNBox groups) instead of
-    // 128 / kNBox 2-D boxes
+    // 128 / kNBox 2-D boxes.  The 3-D map covers columns [0, b3d_cols) -- the
+    // whole column groups; a half that reaches past them (the last tile
+    // column, when N is not a whole number of groups) takes the 2-D boxes of
+    // the second map
     int b3d;
+    int64_t b3d_cols;
     // CTA-pair kernel, stream-K: tiles [0, sk_tiles) of the tile order are
     // cut along K into one contiguous range of K blocks per pair (0 = every
     // tile whole).  A pair that ends inside a tile leaves its raw partial
@@ -1422,8 +1427,8 @@ __device__ __forceinline__ bool sk_init(const Params &p, uint32_t taddr, int64_t
 
 template <int kKind, int kWide, int kRowB>
 __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
-                                              const Params &p, uint32_t smem_base, PairCtrl *ctrl,
-                                              uint32_t rank, WaitCtl *wc)
+                                              const CUtensorMap *tmap_b2, const Params &p, uint32_t smem_base,
+                                              PairCtrl *ctrl, uint32_t rank, WaitCtl *wc)
 {
     using T = Traits<kKind>;
     using S = PairShape<kWide, kRowB>;
@@ -1455,14 +1460,16 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tmap_a, const C
                 const int64_t nb = n0 + w * BN + half * 128;  // this CTA's half of B, MMA w
                 if constexpr (!T::kBNMajor) {
                     ptx::tma_load_2d_pair(sb, tmap_b, full, kc, static_cast<int32_t>(nb));
-                } else if (p.b3d) {
+                } else if (p.b3d && nb + 128 <= p.b3d_cols) {
                     // one instruction instead of four (TF32) or two (16-bit NN):
                     // the producer thread's issue rate bounds the TF32 stage rate
                     ptx::tma_load_3d_pair(sb, tmap_b, full, 0, kc, static_cast<int32_t>(nb / T::kNBox));
                 } else {
+                    // 2-D boxes of one column group each (zeros past N)
+                    const CUtensorMap *m2 = p.b3d ? tmap_b2 : tmap_b;
 #pragma unroll
                     for (int c = 0; c < 128 / T::kNBox; ++c)
-                        ptx::tma_load_2d_pair(sb + c * T::kNBoxBytes, tmap_b, full,
+                        ptx::tma_load_2d_pair(sb + c * T::kNBoxBytes, m2, full,
                                               static_cast<int32_t>(nb + c * T::kNBox), kc);
                 }
             }
@@ -1660,6 +1667,7 @@ template <int kKind, int kWide, int kRowB = ROW_BYTES>
 __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     umma_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_b2,
                      const __grid_constant__ CUtensorMap tmap_c, const Params p)
 {
     static_assert(kRowB == ROW_BYTES || !Traits<kKind>::kBNMajor, "the finer ring is for K-major operands");
@@ -1690,6 +1698,7 @@ __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmap_a);
         ptx::prefetch_tmap(&tmap_b);
+        if (p.b3d) ptx::prefetch_tmap(&tmap_b2);
     }
     if (p.tma_store && warp == 2 && lane == 0) ptx::prefetch_tmap(&tmap_c);
     if (warp == PAIR_MMA_WARP) {
@@ -1704,7 +1713,7 @@ __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     const uint32_t smem_base = ptx::smem_addr(smem);
 
     if (warp == 0) {
-        if (lane == 0) pair_producer<kKind, kWide, kRowB>(&tmap_a, &tmap_b, p, smem_base, ctrl, rank, wc);
+        if (lane == 0) pair_producer<kKind, kWide, kRowB>(&tmap_a, &tmap_b, &tmap_b2, p, smem_base, ctrl, rank, wc);
     } else if (warp == PAIR_MMA_WARP) {
         if (leader) pair_mma<kKind, kWide, kRowB>(p, smem_base, ctrl, tmem_base, rank, lane, wc);
     } else if (warp == PAIR_WAITER_WARP) {
@@ -1914,8 +1923,8 @@ int64_t stream_k_tiles(int64_t tiles, int64_t pairs, int64_t num_kb, double kb_u
 // each).  sk_mode: kSkAuto / kSkOff / kSkOn.
 // *sk tells whether the launch used stream-K.
 template <int kKind, int kWide = 1, int kRowB = ROW_BYTES>
-bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, Params p,
-                 cudaStream_t stream, int sk_mode = kSkOff, bool *sk = nullptr)
+bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mb2, const CUtensorMap &mc,
+                 Params p, cudaStream_t stream, int sk_mode = kSkOff, bool *sk = nullptr)
 {
     if (sk) *sk = false;
     const int clusters = pair_clusters<kKind, kWide, kRowB>();
@@ -1950,7 +1959,7 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
             p.sk_work = w->work;
             p.sk_flags = w->flags;
             p.sk_gen = ++w->gen;
-            if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide, kRowB>, ma, mb, mc, p) != cudaSuccess) {
+            if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide, kRowB>, ma, mb, mb2, mc, p) != cudaSuccess) {
                 cudaGetLastError();
                 return false;
             }
@@ -1961,7 +1970,7 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
         }
     }
     p.sk_tiles = 0;
-    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide, kRowB>, ma, mb, mc, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, umma_pair_kernel<kKind, kWide, kRowB>, ma, mb, mb2, mc, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -1979,6 +1988,7 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, 
     p.bn = BN;
     p.tma_store = 0;
     p.b3d = 0;
+    p.b3d_cols = 0;
     p.sk_tiles = 0;
     p.sk_work = nullptr;
     p.sk_flags = nullptr;
@@ -2248,7 +2258,8 @@ void set_ring(Params &p, bool split)
 // for 128 x bn tiles.
 template <int kKind, typename MakeB>
 const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *mb_pair,
-                         const CUtensorMap *ma_fine, const CUtensorMap *mb_fine, int pair3d, MakeB make_b, const CUtensorMap &mc,
+                         const CUtensorMap *mb_pair2, const CUtensorMap *ma_fine, const CUtensorMap *mb_fine,
+                         int pair3d, int64_t pair3d_cols, MakeB make_b, const CUtensorMap &mc,
                          cudaStream_t stream, const DeviceInfo &dev)
 {
     UmmaConfig cfg = t_tune;
@@ -2279,8 +2290,8 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
                 if (f.bn % box_cols<kKind>() != 0) f.tma_store = 0;
             }
             bool sk = false;
-            const bool ok = wide ? launch_pair<kKind, 2, 64>(*ma_fine, *mb_fine, mc, f, stream, cfg.split, &sk)
-                                 : launch_pair<kKind, 1, 64>(*ma_fine, *mb_fine, mc, f, stream, cfg.split, &sk);
+            const bool ok = wide ? launch_pair<kKind, 2, 64>(*ma_fine, *mb_fine, *mb_fine, mc, f, stream, cfg.split, &sk)
+                                 : launch_pair<kKind, 1, 64>(*ma_fine, *mb_fine, *mb_fine, mc, f, stream, cfg.split, &sk);
             if (ok) return variant_name<kKind>(cfg.variant, BN, 1, sk);
             cfg.variant = wide ? kVariantWide : kVariantPair;
         }
@@ -2288,16 +2299,17 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
     if (cfg.variant == kVariantPair || cfg.variant == kVariantWide) {
         p.tiles_m = (p.M + PAIR_BM - 1) / PAIR_BM;
         p.b3d = pair3d;
+        p.b3d_cols = pair3d_cols;
         bool sk = false;
         if (cfg.variant == kVariantWide) {
             Params w = p;
             w.bn = 2 * BN;  // 256 x 512 pair tiles
             w.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);
             if (w.bn % box_cols<kKind>() != 0) w.tma_store = 0;
-            if (launch_pair<kKind, 2>(ma, *mb_pair, mc, w, stream, cfg.split, &sk))
+            if (launch_pair<kKind, 2>(ma, *mb_pair, *mb_pair2, mc, w, stream, cfg.split, &sk))
                 return variant_name<kKind>(kVariantWide, BN, 1, sk);
         }
-        if (launch_pair<kKind, 1>(ma, *mb_pair, mc, p, stream, cfg.split, &sk))
+        if (launch_pair<kKind, 1>(ma, *mb_pair, *mb_pair2, mc, p, stream, cfg.split, &sk))
             return variant_name<kKind>(kVariantPair, BN, 1, sk);
         cfg = UmmaConfig{kVariantSingle, BN, 1};
         p = p0;
@@ -2380,7 +2392,34 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
         CUtensorMap probe{};
         int probe3d = 0, pair3d = 0;
         if (make_b(BN, &probe, &probe3d)) {
-            const bool ok_pair = make_b(128, &mbp, &pair3d);
+            bool ok_pair = make_b(128, &mbp, &pair3d);
+            // a 3-D map over every column group serves every half (groups past
+            // it read as zeros); mbp2 is then never used
+            int64_t pair3d_cols = pair3d ? INT64_MAX : 0;
+            CUtensorMap mbp2 = mbp;
+            if constexpr (T::kBNMajor) {
+                // N not a whole number of column groups: the pair kernels still
+                // load every tile column but the last with one 3-D box per stage,
+                // from a 3-D map over the whole groups; the last takes 2-D boxes
+                // (mbp, the 2-D map over all of B)
+                const int64_t whole = NB / T::kNBox * T::kNBox;
+                const CUtensorMapSwizzle sw =
+                    T::kTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+                CUtensorMap m3{};
+                if (ok_pair && !pair3d && whole >= 128 &&
+                    make_map_3d(&m3, dt, B,
+                                {static_cast<uint64_t>(T::kNBox), static_cast<uint64_t>(K),
+                                 static_cast<uint64_t>(whole / T::kNBox)},
+                                {static_cast<uint64_t>(ldb * es), static_cast<uint64_t>(T::kNBox * es)},
+                                {static_cast<uint32_t>(T::kNBox), static_cast<uint32_t>(T::BK),
+                                 static_cast<uint32_t>(128 / T::kNBox)},
+                                sw)) {
+                    mbp2 = mbp;
+                    mbp = m3;
+                    pair3d = 1;
+                    pair3d_cols = whole;
+                }
+            }
             // the finer ring (K-major 16-bit kinds, only on request through the
             // tuning hook): 32-element boxes under the 64-byte swizzle
             CUtensorMap maf{}, mbf{};
@@ -2389,8 +2428,9 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
                 if (t_tune.variant == kVariantPairFine || t_tune.variant == kVariantWideFine)
                     ok_fine = make_map(&maf, dt, A, K, M, lda * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) &&
                               make_map(&mbf, dt, B, K, N, ldb * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
-            return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, ok_fine ? &maf : nullptr,
-                                       ok_fine ? &mbf : nullptr, pair3d, make_b, mc, stream, dev);
+            return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, ok_pair ? &mbp2 : nullptr,
+                                       ok_fine ? &maf : nullptr, ok_fine ? &mbf : nullptr, pair3d, pair3d_cols,
+                                       make_b, mc, stream, dev);
         }
     }
     t_tune = UmmaConfig{kVariantAuto, BN, 1};

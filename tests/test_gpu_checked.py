@@ -102,6 +102,26 @@ def test_kernel_families_pass_every_check(Lc, path, shape, pad, tune, frag):
     assert frag in name, name
 
 
+def test_fuzz_cases_pass_every_check(Lc):
+    """Every fourth seeded case of the general fuzz (all paths, pitch padding,
+    base offsets, forced tile configurations) through the checked library."""
+    import dense_gemm_09_gb300 as dg
+    from tests.test_gpu_fuzz import CASES
+    for path, (M, N, K), pad, offset, alpha, beta, tune in CASES[::4]:
+        A, B, C = parity.host_operands(path, M, N, K, seed=M * 7 + N * 13 + K)
+        dA, _ = parity.to_device_padded(A, pad[0], offset_elems=offset[0])
+        dB, _ = parity.to_device_padded(B, pad[1], offset_elems=offset[1])
+        dC, _ = parity.to_device_padded(C, pad[2], fill=float("nan") if pad[2] else 0.0, offset_elems=offset[2])
+        if tune[0] != 0:
+            assert Lc.dgemm_tune_next(*tune) == dg.OK
+        assert _call(Lc, path, dA, dB, dC, alpha, beta) == dg.OK
+        st, site = Lc.dgemm_device_status(0), Lc.dgemm_check_site()
+        Lc.dgemm_device_status(1)
+        name = Lc.dgemm_last_kernel().decode()
+        assert st == dg.OK and site == 0, "%s %s: %s at site %d" % (path, (M, N, K), name, site)
+        assert parity.worst_ratio(path, dC.cpu(), A, B, C, alpha, beta) <= 1.0, name
+
+
 def test_workspace_copies_pass_every_check(Lc):
     import dense_gemm_09_gb300 as dg
     M, N, K = 301, 257, 129

@@ -421,6 +421,24 @@ def test_simt_split_unaligned_b():
     assert parity.worst_ratio("f32", got, A, B, C, 1.5, -0.25) <= 1.0
 
 
+# N-major B (TF32 and the NN 16-bit kinds) whose N is not a whole number of
+# 128-byte column groups: the pair kernels load every tile column but the
+# last with one 3-D box per stage, and the last one with 2-D boxes.
+@pytest.mark.parametrize("path", ["tf32", "f16_nn", "bf16_nn"])
+# (N a multiple of 8 but not of 64: TMA-describable pitches for every kind)
+@pytest.mark.parametrize("shape", [(600, 4088, 256), (520, 1096, 300), (300, 520, 264)])
+@pytest.mark.parametrize("wide", [False, True], ids=["256x256", "256x512"])
+def test_n_major_ragged_n_pair(path, shape, wide):
+    import dense_gemm_09_gb300 as dg
+    M, N, K = shape
+    A, B, C = parity.host_operands(path, M, N, K, seed=M + 2 * N + K)
+    dg.tune_next(dg.TUNE_PAIR_WIDE if wide else dg.TUNE_PAIR, 256, dg.SK_OFF)
+    got, _, _ = parity.run(path, A, B, C, 1.25, -0.5)
+    assert "_pair_" in dg.last_kernel(), dg.last_kernel()
+    assert dg.device_status() == dg.OK
+    assert parity.worst_ratio(path, got, A, B, C, 1.25, -0.5) <= 1.0
+
+
 # FP32 SIMT fed by TMA: problems of at least a wave of tiles whose A and B
 # have 16-byte aligned bases and pitches.  Tails in M, N and K come from TMA's
 # zero fill and the epilogue's masks; a C pitch that is not a multiple of 4
