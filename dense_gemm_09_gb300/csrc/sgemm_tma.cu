@@ -113,8 +113,9 @@ __device__ __forceinline__ bool aborted(const int *abort)
 
 // The slow part of wait_phase: poll until the phase completes, the limit
 // runs out (which raises the abort flag and records DGEMM_ERR_TIMEOUT) or
-// another warp raised the flag.
-__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, int *abort, uint64_t limit_ns)
+// another warp raised the flag.  Inlined: a call inside the main loop would
+// constrain the register allocation of the ~210 registers live there.
+__device__ __forceinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, int *abort, uint64_t limit_ns)
 {
     const uint64_t t0 = ptx::globaltimer_ns();
     for (;;) {

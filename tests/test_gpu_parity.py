@@ -425,8 +425,9 @@ def test_simt_split_unaligned_b():
 # 128-byte column groups: the pair kernels load every tile column but the
 # last with one 3-D box per stage, and the last one with 2-D boxes.
 @pytest.mark.parametrize("path", ["tf32", "f16_nn", "bf16_nn"])
-# (N a multiple of 8 but not of 64: TMA-describable pitches for every kind)
-@pytest.mark.parametrize("shape", [(600, 4088, 256), (520, 1096, 300), (300, 520, 264)])
+# (N a multiple of 8 but not of 64, K a multiple of 8: TMA-describable pitches
+# for every kind; K = 312 also leaves a partial last K block)
+@pytest.mark.parametrize("shape", [(600, 4088, 256), (520, 1096, 312), (300, 520, 264)])
 @pytest.mark.parametrize("wide", [False, True], ids=["256x256", "256x512"])
 def test_n_major_ragged_n_pair(path, shape, wide):
     import dense_gemm_09_gb300 as dg
