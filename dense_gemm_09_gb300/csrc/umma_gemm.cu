@@ -205,8 +205,10 @@ struct Params {
     // kernels use 256.  The MMA is 128 x bn x UMMA_K.
     int bn;
     // single-CTA kernel: stages in its ring and bytes per stage (1024-byte
-    // multiples); the TMA producer uses A_TILE_BYTES + bn * ROW_BYTES
-    int stages, stage_bytes;
+    // multiples).  The TMA producer fills a stage with kpb K blocks (1 or 2),
+    // each A_TILE_BYTES of A then bn * ROW_BYTES of B; the non-TMA producers
+    // use one K block of STAGE_BYTES
+    int stages, stage_bytes, kpb;
     // CTA-pair kernel with N-major B: the stage's B half comes as one 3-D box
     // (column group of 128 bytes x BK rows x 128 / kNBox groups) instead of
     // 128 / kNBox 2-D boxes.  The 3-D map covers columns [0, b3d_cols) -- the
@@ -328,7 +330,7 @@ __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity)
     return true;
 }
 
-template <int kKind>
+template <int kKind, int kKpb>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
                                              const Params &p, uint32_t smem_base, Ctrl *ctrl,
                                              WaitCtl *wc)
@@ -342,29 +344,37 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmap_a, const CU
     for (int64_t t = sc.t0; ok && t < num_tiles; t += sc.dt) {
         int64_t m0, n0;
         tile_coords(t, p, m0, n0);
-        for (int64_t kb = sc.kb0; kb < sc.kb1; ++kb) {
+        for (int64_t kb = sc.kb0; kb < sc.kb1; kb += kKpb) {
             if (!wait_bounded(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
                 ok = false;
                 break;
             }
+            // K blocks kb and (two per stage, if inside the range) kb + 1,
+            // one after the other in the stage
+            const bool second = kKpb == 2 && kb + 1 < sc.kb1;
+            const uint32_t half = A_TILE_BYTES + static_cast<uint32_t>(p.bn) * ROW_BYTES;
             const uint32_t full = ptx::smem_addr(&ctrl->full[stage]);
-            ptx::mbar_arrive_expect_tx(full, A_TILE_BYTES + p.bn * ROW_BYTES);
-            const uint32_t sa = smem_base + stage * static_cast<uint32_t>(p.stage_bytes);
-            const uint32_t sb = sa + A_TILE_BYTES;
-            const int32_t kc = static_cast<int32_t>(kb * T::BK);
-            ptx::tma_load_2d(sa, tmap_a, full, kc, static_cast<int32_t>(m0));
-            if constexpr (!T::kBNMajor) {
-                ptx::tma_load_2d(sb, tmap_b, full, kc, static_cast<int32_t>(n0));
-            } else if (p.b3d) {
-                // B is N-major, all bn / kNBox column groups in one 3-D box
-                ptx::tma_load_3d(sb, tmap_b, full, 0, kc, static_cast<int32_t>(n0 / T::kNBox));
-            } else {
-                // B is N-major: boxes of 128 bytes of columns x BK rows, one
-                // swizzle column each (see Traits)
+            ptx::mbar_arrive_expect_tx(full, second ? 2 * half : half);
+#pragma unroll
+            for (int h = 0; h < kKpb; ++h) {
+                if (h == 1 && !second) break;
+                const uint32_t sa = smem_base + stage * static_cast<uint32_t>(p.stage_bytes) + h * half;
+                const uint32_t sb = sa + A_TILE_BYTES;
+                const int32_t kc = static_cast<int32_t>((kb + h) * T::BK);
+                ptx::tma_load_2d(sa, tmap_a, full, kc, static_cast<int32_t>(m0));
+                if constexpr (!T::kBNMajor) {
+                    ptx::tma_load_2d(sb, tmap_b, full, kc, static_cast<int32_t>(n0));
+                } else if (p.b3d) {
+                    // B is N-major, all bn / kNBox column groups in one 3-D box
+                    ptx::tma_load_3d(sb, tmap_b, full, 0, kc, static_cast<int32_t>(n0 / T::kNBox));
+                } else {
+                    // B is N-major: boxes of 128 bytes of columns x BK rows, one
+                    // swizzle column each (see Traits)
 #pragma unroll 1
-                for (int c = 0; c < p.bn / T::kNBox; ++c)
-                    ptx::tma_load_2d(sb + c * T::kNBoxBytes, tmap_b, full,
-                                     static_cast<int32_t>(n0 + c * T::kNBox), kc);
+                    for (int c = 0; c < p.bn / T::kNBox; ++c)
+                        ptx::tma_load_2d(sb + c * T::kNBoxBytes, tmap_b, full,
+                                         static_cast<int32_t>(n0 + c * T::kNBox), kc);
+                }
             }
             issued |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -565,7 +575,7 @@ __device__ __forceinline__ void run_cpasync_producer(const Params &p, uint32_t s
     for (int q = 0; q < npending; ++q) ptx::mbar_arrive(ptx::smem_addr(&ctrl->full[pending[q]]));
 }
 
-template <int kKind, bool kTma>
+template <int kKind, bool kTma, int kKpb>
 __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctrl *ctrl,
                                         uint32_t tmem_base, WaitCtl *wc)
 {
@@ -583,30 +593,35 @@ __device__ __forceinline__ void run_mma(const Params &p, uint32_t smem_base, Ctr
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int64_t kb = sc.kb0; kb < sc.kb1; ++kb) {
+        for (int64_t kb = sc.kb0; kb < sc.kb1; kb += kKpb) {
             if (!wait_bounded(ptx::smem_addr(&ctrl->full[stage]), phase, wc)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t sa = smem_base + stage * static_cast<uint32_t>(p.stage_bytes);
-            const uint32_t sb = sa + A_TILE_BYTES;
+            const bool second = kKpb == 2 && kb + 1 < sc.kb1;
 #pragma unroll
-            for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
-                // A (K-major): advance 32 bytes along the swizzled row; 8-row
-                // groups of the tile are 1024 bytes apart.
-                const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
-                uint64_t db;
-                if constexpr (!T::kBNMajor || !kTma) {
-                    // B staged K-major like A
-                    db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
-                } else {
-                    // B N-major: one MMA's K rows per step; boxes of 128
-                    // bytes of columns are kNBoxBytes apart
-                    db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
+            for (int h = 0; h < kKpb; ++h) {
+                if (h == 1 && !second) break;
+                const uint32_t sa = smem_base + stage * static_cast<uint32_t>(p.stage_bytes) +
+                                    h * (A_TILE_BYTES + static_cast<uint32_t>(p.bn) * ROW_BYTES);
+                const uint32_t sb = sa + A_TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
+                    // A (K-major): advance 32 bytes along the swizzled row; 8-row
+                    // groups of the tile are 1024 bytes apart.
+                    const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
+                    uint64_t db;
+                    if constexpr (!T::kBNMajor || !kTma) {
+                        // B staged K-major like A
+                        db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
+                    } else {
+                        // B N-major: one MMA's K rows per step; boxes of 128
+                        // bytes of columns are kNBoxBytes apart
+                        db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
+                    }
+                    ptx::umma<kKind>(d_tmem, da, db, idesc, (kb + h != sc.kb0 || k != 0) ? 1u : 0u);
                 }
-                ptx::umma<kKind>(d_tmem, da, db, idesc,
-                                 (kb != sc.kb0 || k != 0) ? 1u : 0u);
             }
             ptx::umma_commit(ptx::smem_addr(&ctrl->empty[stage]));
             if (++stage == static_cast<uint32_t>(p.stages)) {
@@ -1051,7 +1066,11 @@ constexpr int cta_threads()
     return 32 * (producer_warps<kTma>() + 1 + 4);
 }
 
-template <int kKind, bool kTma>
+// kKpb: K blocks per stage of the TMA producer (p.kpb; 1 for the non-TMA
+// producers).  Two instances rather than a run-time count: the one-block
+// kernel keeps the code (and the cold-start instruction fetches) of a
+// single block per stage.
+template <int kKind, bool kTma, int kKpb = 1>
 __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
@@ -1097,14 +1116,14 @@ __global__ void __launch_bounds__(cta_threads<kTma>(), 1)
 
     if (warp < kMmaWarp) {
         if constexpr (kTma) {
-            if (lane == 0) run_producer<kKind>(&tmap_a, &tmap_b, p, smem_base, ctrl, wc);
+            if (lane == 0) run_producer<kKind, kKpb>(&tmap_a, &tmap_b, p, smem_base, ctrl, wc);
         } else if constexpr (kKind == kTF32) {
             run_cpasync_producer(p, smem_base, ctrl, threadIdx.x, wc);
         } else {
             run_reg_producer<kKind>(p, smem_base, ctrl, threadIdx.x, wc);
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) run_mma<kKind, kTma>(p, smem_base, ctrl, tmem_base, wc);
+        if (lane == 0) run_mma<kKind, kTma, kKpb>(p, smem_base, ctrl, tmem_base, wc);
     } else {
         if (p.splitk > 1)
             splitk_wait_acc(ctrl, wc);
@@ -1786,13 +1805,15 @@ template <int kKind, bool kTma>
 bool launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const Params &p,
             cudaStream_t stream, const DeviceInfo &dev)
 {
-    if (cudaFuncSetAttribute(umma_gemm_kernel<kKind, kTma>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+    // the TMA kernel with two K blocks per stage is its own instance
+    auto kernel = umma_gemm_kernel<kKind, kTma, 1>;
+    if constexpr (kTma)
+        if (p.kpb == 2) kernel = umma_gemm_kernel<kKind, true, 2>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
         return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
     const int64_t grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-    umma_gemm_kernel<kKind, kTma>
-        <<<static_cast<unsigned>(grid), cta_threads<kTma>(), SMEM_BYTES, stream>>>(ma, mb, mc, p);
+    kernel<<<static_cast<unsigned>(grid), cta_threads<kTma>(), SMEM_BYTES, stream>>>(ma, mb, mc, p);
     return true;
 }
 
@@ -1995,6 +2016,7 @@ Params make_params(int64_t M, int64_t N, int64_t K, float alpha, const void *A, 
     p.sk_gen = 0;
     p.stages = STAGES;
     p.stage_bytes = STAGE_BYTES;
+    p.kpb = 1;
     const uint64_t stall = take_injected_stall();
     p.inject_stall = stall ? 1 : 0;
     p.splitk = 1;
@@ -2178,8 +2200,8 @@ template <int kKind>
 bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
                    const Params &p, cudaStream_t stream)
 {
-    if (cudaFuncSetAttribute(umma_gemm_kernel<kKind, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
+    auto kernel = p.kpb == 2 ? umma_gemm_kernel<kKind, true, 2> : umma_gemm_kernel<kKind, true, 1>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -2195,7 +2217,7 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorM
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, umma_gemm_kernel<kKind, true>, ma, mb, mc, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, ma, mb, mc, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -2242,14 +2264,24 @@ const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = fals
     return names[2 + w * 9 + S].c_str();
 }
 
-// The single-CTA TMA kernel's ring for tile width p.bn: as many stages of
-// A_TILE_BYTES + bn * ROW_BYTES as fit in the ring space (at most
-// MAX_STAGES).  Split-K launches do not use the epilogue boxes (their
-// partials meet in the ring), so their ring may extend over them.
+// The single-CTA TMA kernel's ring for tile width p.bn: as many stages as
+// fit in the ring space (at most MAX_STAGES), each of kpb K blocks of
+// A_TILE_BYTES + bn * ROW_BYTES.  Two K blocks per stage for tiles up to
+// 128 wide (a block's B at most 16 KB).  Measured on GB300, a plain TMA
+// stream whose stages carry 16 KB runs ~20 % slower than one whose stages
+// carry 32 KB, however many stages are in flight: a fixed cost per stage,
+// which the deeper stages halve (with the kernel's code cached: 256^3 FP16
+// 10.2 -> 8.6 us, 1024^3 14.3 -> 12.3 us, 512 x 512 x 8192 22.5 -> 20.6 us,
+// TF32 64 x 2048 x 8192 28.6 -> 25.9 us; at 160 wide, three stages of two
+// blocks were slower than five of one).  Split-K launches do not use the
+// epilogue boxes (their partials meet in the ring), so their ring may extend
+// over them.
 void set_ring(Params &p, bool split)
 {
-    p.stage_bytes = A_TILE_BYTES + p.bn * ROW_BYTES;
+    const int half = A_TILE_BYTES + p.bn * ROW_BYTES;
     const int space = STAGES * STAGE_BYTES + (split ? EPI_BYTES : 0);
+    p.kpb = p.bn * ROW_BYTES <= 16 * 1024 ? 2 : 1;
+    p.stage_bytes = p.kpb * half;
     p.stages = std::min(MAX_STAGES, space / p.stage_bytes);
 }
 

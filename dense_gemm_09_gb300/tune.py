@@ -14,6 +14,12 @@ sweeps.
 With --cublas it also times torch.matmul (cuBLAS) on the same operands and
 flush, as a context line; cuBLAS is never part of the library's path.
 
+--flush clean (the default, as in bench.py) zeroes a 512 MB buffer and then
+reads another 512 MB before every timed call, so the L2 holds none of the
+operands and only clean lines.  --flush write only zeroes the buffer, which
+leaves the L2 full of dirty lines: the timed call then also pays for their
+write-back (~5 us for a 100 MB HBM-bound call on GB300).
+
 Operands are seeded uniform[-1, 1) values on the current GPU; the L2 cache
 is flushed before every timed call, and times are means of CUDA-event
 intervals (the event clock ticks in steps of about 2 us, so means resolve
@@ -43,8 +49,8 @@ def configs(step: int, sms: int, M: int, N: int):
         return [(dg.TUNE_AUTO, 256, 1)]
     """Every (variant, bn, split) worth timing: the pair kernels (256 x 256
     and 256 x 512 tiles, each round-robin and with the stream-K tail, with
-    the ordinary and the finer stage ring), and for each tile width bn the single-CTA kernel and
-    the splits that fit one wave (step 0: the FP32 SIMT call, automatic
+    the ordinary and the finer stage ring), and for each tile width bn the single-CTA kernel
+    and the splits that fit one wave (step 0: the FP32 SIMT call, automatic
     only)."""
     out = [(dg.TUNE_AUTO, 256, 1), (dg.TUNE_PAIR, 256, dg.SK_OFF), (dg.TUNE_PAIR, 256, dg.SK_ON),
            (dg.TUNE_PAIR_WIDE, 256, dg.SK_OFF),
@@ -70,7 +76,8 @@ def cublas_call(kind: str, A, B, out):
 
 
 def sweep(kind: str, M: int, N: int, K: int, reps: int = 30, warmup: int = 3, seed: int = 0,
-          cublas: bool = False, cublas_only: bool = False, profile_range: bool = False):
+          cublas: bool = False, cublas_only: bool = False, profile_range: bool = False,
+          flush_mode: str = "clean"):
     dtype, tn, fn, step = KINDS[kind]
     dev = torch.device("cuda")
     g = torch.Generator().manual_seed(seed)
@@ -79,6 +86,7 @@ def sweep(kind: str, M: int, N: int, K: int, reps: int = 30, warmup: int = 3, se
     B = (torch.rand(Bshape, generator=g) * 2 - 1).to(dtype).to(dev)
     C = torch.empty((M, N), dtype=dtype, device=dev)
     flush = torch.empty(512 * 2**20 // 4, device=dev)
+    flush_read = torch.ones(512 * 2**20 // 4, device=dev) if flush_mode == "clean" else None
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ref = None
     rows = []
@@ -99,6 +107,8 @@ def sweep(kind: str, M: int, N: int, K: int, reps: int = 30, warmup: int = 3, se
         times = []
         for _ in range(reps):
             flush.zero_()
+            if flush_read is not None:
+                flush_read.sum()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -139,12 +149,15 @@ def main():
     ap.add_argument("--profile-range", action="store_true",
                     help="bracket each timed call with the profiler start/stop API, so that "
                          "ncu --profile-from-start off captures those launches and nothing else")
+    ap.add_argument("--flush", choices=("clean", "write"), default="clean",
+                    help="clean: zero 512 MB, then read another 512 MB before each call (as the bench); "
+                         "write: only zero it, leaving dirty lines in L2")
     a = ap.parse_args()
     M, N, K = (int(v) for v in a.shape.lower().split("x"))
     table = sweep(a.kind, M, N, K, reps=a.reps, cublas=a.cublas, cublas_only=a.cublas_only,
-                  profile_range=a.profile_range)
+                  profile_range=a.profile_range, flush_mode=a.flush)
     flops = 2.0 * M * N * K
-    print("%s %dx%dx%d" % (a.kind, M, N, K))
+    print("%s %dx%dx%d (flush: %s)" % (a.kind, M, N, K, a.flush))
     for ms, name, auto, diff in table:
         print("  %-44s %9.4f ms %9.2f TFLOP/s  max rel diff %.1e%s"
               % (name, ms, flops / ms / 1e9, diff, "   <- automatic" if auto else ""))
