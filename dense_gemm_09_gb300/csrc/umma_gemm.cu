@@ -2116,15 +2116,19 @@ constexpr int bn_step()
 //   * candidates: bn from 256 down in the kind's step (32, or 64 for the
 //     16-bit NN kinds); S from 1 to 8 with at least 8 K blocks per rank,
 //     tiles * S <= SMs, and all clusters resident at once;
-//   * estimated time per CTA = its K blocks x max(MMA time, load time) +
+//   * estimated time = its K blocks x max(MMA time, load time) per CTA +
 //     the cost of adding S partials, with the load time of a K block
-//     (128 + bn rows of 128 bytes) at a per-SM stream rate and the whole
-//     launch no faster than the operands at the HBM rate;
+//     (128 + bn rows of 128 bytes) at a per-CTA stream rate, and the whole
+//     launch no faster than the operands at the HBM rate nor than all the
+//     CTAs' stage bytes at an aggregate L2 -> SM rate;
 //   * the smallest estimate wins (ties: the wider tile, the smaller S).
 // The constants are fitted to GB300 sweeps of the tuning tool
-// (dense_gemm_09_gb300/tune.py): an MMA K block of 128 x 256 x 128 bytes in
-// ~0.33 us, a CTA streams ~75 GB/s, HBM ~6 TB/s; a split costs ~1 us plus
-// ~0.5 us per extra rank plus ~0.9 us per 64 KB of partials moved.
+// (dense_gemm_09_gb300/tune.py, 15 shapes; every automatic choice within
+// 2 % of the best configuration measured): an MMA K block of 128 x 256 x
+// 128 bytes in ~0.33 us; a CTA streams ~65 GB/s with one K block per stage
+// and ~100 GB/s with two (tiles up to 128 wide, see set_ring); HBM ~6 TB/s;
+// L2 -> SM ~10 TB/s in all; a split costs ~1 us plus ~0.25 us per extra
+// rank plus ~0.5 us per 64 KB of partials moved.
 template <int kKind>
 UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok)
 {
@@ -2173,20 +2177,25 @@ UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok)
     }
     if (tiles256 * 2 > sm_count) return {kVariantSingle, BN, 1};
     const double kb_mma_us = 0.33 / 256.0;          // per column of bn, one K block
-    const double sm_bytes_per_us = 75e3;            // 75 GB/s
+    const double cta_bytes_per_us_1 = 65e3;         // 65 GB/s, one K block per stage
+    const double cta_bytes_per_us_2 = 100e3;        // 100 GB/s, two (bn <= 128)
     const double hbm_bytes_per_us = 6.0e6;          // 6 TB/s
+    const double l2_bytes_per_us = 10.0e6;          // 10 TB/s, L2 -> all SMs
     const double operand_bytes = static_cast<double>(p.M * p.K + p.N * p.K) * T::kElem;
     UmmaConfig best{kVariantSingle, BN, 1};
     double best_t = 1e30;
     for (int bn = BN; bn >= bn_step<kKind>(); bn -= bn_step<kKind>()) {
         const int64_t tiles = p.tiles_m * ((p.N + bn - 1) / bn);
+        const double rate = bn * ROW_BYTES <= 16 * 1024 ? cta_bytes_per_us_2 : cta_bytes_per_us_1;
         for (int S = 1; S <= 8; ++S) {
             if (tiles * S > sm_count) break;
             if (S > 1 && (p.num_kb < 8 * S || tiles > cluster_capacity<kKind>(S))) continue;
             const int64_t kb = (p.num_kb + S - 1) / S;
-            const double t_kb = std::max(kb_mma_us * bn, (BM + bn) * 128.0 / sm_bytes_per_us);
-            double t = std::max(kb * t_kb, operand_bytes / hbm_bytes_per_us);
-            if (S > 1) t += 1.0 + 0.5 * (S - 1) + 0.9 * (BM * bn * 4.0 / 65536.0) * (S - 1) / S;
+            const double kb_bytes = (BM + bn) * 128.0;
+            const double t_kb = std::max(kb_mma_us * bn, kb_bytes / rate);
+            double t = std::max({kb * t_kb, operand_bytes / hbm_bytes_per_us,
+                                 static_cast<double>(tiles * S * kb) * kb_bytes / l2_bytes_per_us});
+            if (S > 1) t += 1.0 + 0.25 * (S - 1) + 0.5 * (BM * bn * 4.0 / 65536.0) * (S - 1) / S;
             if (t < best_t * 0.98) {
                 best_t = t;
                 best = {S > 1 ? kVariantSplit : kVariantSingle, bn, S};
