@@ -129,6 +129,8 @@ def test_inject_stall(wait_limit_ns: int) -> None:
 TUNE_AUTO, TUNE_PAIR, TUNE_SINGLE, TUNE_SPLIT, TUNE_PAIR_WIDE = 0, 1, 2, 3, 5
 # the CTA-pair variants with the finer stage ring (K-major 16-bit calls)
 TUNE_PAIR_FINE, TUNE_PAIR_WIDE_FINE = 6, 7
+# the CTA pair for small M: 128 x bn tiles (bn 128, 192 or 256), 64 rows of A per CTA
+TUNE_PAIR128 = 8
 # `split` of the CTA-pair variants (TUNE_PAIR, TUNE_PAIR_WIDE): stream-K tail
 # chosen automatically, never, or whenever the tiles outnumber the pairs
 SK_AUTO, SK_OFF, SK_ON = 0, 1, 2
@@ -137,7 +139,7 @@ SK_AUTO, SK_OFF, SK_ON = 0, 1, 2
 def tune_next(variant: int, bn: int = 256, split: int = 1) -> None:
     """Tuning hook: fix the tile configuration of the next tensor-core call
     on this thread (variant TUNE_PAIR / TUNE_PAIR_WIDE / TUNE_PAIR_FINE /
-    TUNE_PAIR_WIDE_FINE / TUNE_SINGLE / TUNE_SPLIT, tile width bn, split-K
+    TUNE_PAIR_WIDE_FINE / TUNE_SINGLE / TUNE_SPLIT / TUNE_PAIR128, tile width bn, split-K
     factor split; for the pair variants, split is the stream-K mode SK_*)."""
     st = lib().dgemm_tune_next(int(variant), int(bn), int(split))
     if st != OK:

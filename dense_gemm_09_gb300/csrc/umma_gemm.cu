@@ -1752,6 +1752,228 @@ __global__ void __launch_bounds__(pair_threads<kWide>(), 1)
     }
 }
 
+// ------------------------------------------------- CTA pairs for small M
+//
+// Problems of few rows (skinny M, a long K) are bound by the bytes every
+// CTA pulls into shared memory: each CTA of the single-CTA kernel reloads
+// all 128 rows of A for its 128 x bn tile.  Here a CTA pair shares one
+// tcgen05.mma of M = 128 (cta_group::2): each CTA loads 64 rows of A and
+// bn / 2 rows (or columns, N-major) of B per K block, so a tile of 128 x bn
+// costs each CTA (64 + bn / 2) rows per K block instead of 128 + bn.  The
+// accumulator of M = 128 lies in each CTA's TMEM as its 64 rows twice over:
+// lanes 0-63 hold columns [0, bn / 2) and lanes 64-127 columns [bn / 2, bn),
+// both in TMEM columns 0 .. bn / 2 - 1 (measured on GB300).
+//   both CTAs  warp 0: TMA producer into the CTA's ring, two K blocks per
+//              stage; both CTAs' loads complete on the leader's "full"
+//              barrier, armed by the leader with the bytes of both;
+//              warps 2-5: epilogue, warp w drains TMEM lane quarter w mod 4:
+//              rows 32 (q mod 2) .. of the CTA's 64, column half q / 2;
+//   leader     warp 1: the MMA issuer (one lane), committing each stage's
+//              release to both CTAs' "empty" barriers and the finished
+//              accumulator to both CTAs' "tmem_full".
+// One tile per pair (a grid of 2 x tiles CTAs, at most one wave of pairs).
+// p.bn is the tile width: 128, 192 or 256 (a multiple of 64 whose half is a
+// whole number of B boxes); p.tiles_m counts 128-row bands.
+
+constexpr int P128_A_BYTES = 64 * ROW_BYTES;  // 8 KB: this CTA's 64 rows of A, one K block
+constexpr int P128_TMEM_COLS = 128;           // bn / 2 <= 128 accumulator columns
+
+template <int kKind>
+constexpr uint32_t p128_idesc(int bn)
+{
+    return (Traits<kKind>::kIdesc & ~(0x3Fu << 17) & ~(0x1Fu << 24)) |
+           (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+// Bytes one CTA loads for one K block (A rows, then B rows or columns).
+__host__ __device__ constexpr uint32_t p128_half_bytes(int bn)
+{
+    return static_cast<uint32_t>(P128_A_BYTES + (bn / 2) * ROW_BYTES);
+}
+
+template <int kKind>
+__device__ __forceinline__ void p128_producer(const CUtensorMap *tmap_a, const CUtensorMap *tmap_b,
+                                              const CUtensorMap *tmap_b2, const Params &p, uint32_t smem_base,
+                                              Ctrl *ctrl, uint32_t rank, WaitCtl *wc)
+{
+    using T = Traits<kKind>;
+    const int64_t t = blockIdx.x / 2;
+    const int64_t m0 = (t % p.tiles_m) * BM, n0 = (t / p.tiles_m) * p.bn;
+    const int64_t mh = m0 + rank * 64, nb = n0 + rank * (p.bn / 2);  // this CTA's rows of A, of B
+    const uint32_t half = p128_half_bytes(p.bn);
+    uint32_t stage = 0, phase = 0, issued = 0, issued_phase = 0;
+    bool ok = true;
+    for (int64_t kb = 0; kb < p.num_kb; kb += 2) {
+        if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->empty[stage]), phase ^ 1u, wc)) {
+            ok = false;
+            break;
+        }
+        const bool second = kb + 1 < p.num_kb;
+        const uint32_t full_local = ptx::smem_addr(&ctrl->full[stage]);
+        const uint32_t full = ptx::mapa(full_local, 0);  // the leader's barrier
+        if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, (second ? 4u : 2u) * half);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h == 1 && !second) break;
+            const uint32_t sa = smem_base + stage * static_cast<uint32_t>(p.stage_bytes) + h * half;
+            const uint32_t sb = sa + P128_A_BYTES;
+            const int32_t kc = static_cast<int32_t>((kb + h) * T::BK);
+            ptx::tma_load_2d_pair(sa, tmap_a, full, kc, static_cast<int32_t>(mh));
+            if constexpr (!T::kBNMajor) {
+                ptx::tma_load_2d_pair(sb, tmap_b, full, kc, static_cast<int32_t>(nb));
+            } else if (p.b3d && nb + p.bn / 2 <= p.b3d_cols) {
+                ptx::tma_load_3d_pair(sb, tmap_b, full, 0, kc, static_cast<int32_t>(nb / T::kNBox));
+            } else {
+                const CUtensorMap *m2 = p.b3d ? tmap_b2 : tmap_b;
+#pragma unroll 1
+                for (int c = 0; c < p.bn / 2 / T::kNBox; ++c)
+                    ptx::tma_load_2d_pair(sb + c * T::kNBoxBytes, m2, full,
+                                          static_cast<int32_t>(nb + c * T::kNBox), kc);
+            }
+        }
+        issued |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+    if (!ok && rank == 0) {
+        // the leader's barriers count both CTAs' bytes: wait (bounded) for
+        // the loads in flight before the pair leaves
+        for (int s = 0; s < p.stages; ++s)
+            if ((issued >> s) & 1u) drain_wait(ptx::smem_addr(&ctrl->full[s]), (issued_phase >> s) & 1u);
+    }
+}
+
+template <int kKind>
+__device__ __forceinline__ void p128_mma(const Params &p, uint32_t smem_base, Ctrl *ctrl, uint32_t tmem_base,
+                                         WaitCtl *wc)
+{
+    using T = Traits<kKind>;
+    constexpr uint16_t kBoth = 0x3;
+    const uint32_t half = p128_half_bytes(p.bn);
+    const uint32_t idesc = p128_idesc<kKind>(p.bn);
+    uint32_t stage = 0, phase = 0;
+    bool ok = !p.inject_stall || wait_bounded(ptx::smem_addr(&ctrl->never), 0, wc);
+    for (int64_t kb = 0; ok && kb < p.num_kb; kb += 2) {
+        if (!wait_bounded_cluster(ptx::smem_addr(&ctrl->full[stage]), phase, wc)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        const bool second = kb + 1 < p.num_kb;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h == 1 && !second) break;
+            const uint32_t sa = smem_base + stage * static_cast<uint32_t>(p.stage_bytes) + h * half;
+            const uint32_t sb = sa + P128_A_BYTES;
+#pragma unroll
+            for (int k = 0; k < T::BK / T::UMMA_K; ++k) {
+                const uint64_t da = ptx::smem_desc(sa + k * 32, 16, 1024, ptx::kSw128);
+                uint64_t db;
+                if constexpr (!T::kBNMajor)
+                    db = ptx::smem_desc(sb + k * 32, 16, 1024, ptx::kSw128);
+                else
+                    db = ptx::smem_desc(sb + k * T::kNStep, T::kNBoxBytes, T::kNSbo, T::kNLayout);
+                ptx::umma_pair<kKind>(tmem_base, da, db, idesc, (kb + h != 0 || k != 0) ? 1u : 0u);
+            }
+        }
+        ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->empty[stage]), kBoth);
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+    if (ok) ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->tmem_full[0]), kBoth);
+    // every MMA this thread issued has finished before TMEM can be released
+    ptx::umma_commit_pair_multicast(ptx::smem_addr(&ctrl->mma_done), 0x1);
+    drain_wait(ptx::smem_addr(&ctrl->mma_done), 0);
+}
+
+template <int kKind>
+__device__ __forceinline__ void p128_epilogue(const Params &p, const CUtensorMap *tmap_c, Ctrl *ctrl,
+                                              uint32_t tmem_base, uint32_t epi_smem, uint32_t rank, int warp,
+                                              int lane, WaitCtl *wc)
+{
+    const int64_t t = blockIdx.x / 2;
+    const int64_t m0 = (t % p.tiles_m) * BM, n0 = (t / p.tiles_m) * p.bn;
+    const uint32_t q = static_cast<uint32_t>(warp & 3);  // the TMEM lane quarter this warp may read
+    const int cols = p.bn / 2;
+    const int64_t row0 = m0 + rank * 64 + (q & 1u) * 32, col0 = n0 + (q >> 1) * cols;
+    bool ok = wait_bounded_cluster(ptx::smem_addr(&ctrl->tmem_full[0]), 0, wc);
+    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+    if (ok) {
+        ptx::tc_fence_after();
+        uint32_t nbox = 0;
+        // the tile lies inside C and the columns inside the allocation (warp-uniform)
+        if (DGEMM_CHECK(m0 >= 0 && m0 < p.M && n0 >= 0 && n0 < p.N && cols <= P128_TMEM_COLS))
+            drain_rows<kKind>(p, tmap_c, tmem_base + ((q * 32u) << 16), row0, col0,
+                              epi_smem + q * 2 * EPI_BOX_BYTES, lane, nbox, cols);
+    }
+    if (lane == 0) ptx::bulk_wait<0>();  // stores done before the CTA leaves
+}
+
+template <int kKind>
+__global__ void __launch_bounds__(cta_threads<true>(), 1)
+    umma_pair128_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                        const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_c,
+                        const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank() & 1u;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < MAX_STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&ctrl->full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctrl->empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(&ctrl->tmem_full[0]), 1);
+        ptx::mbar_init(ptx::smem_addr(&ctrl->mma_done), 1);
+        ptx::mbar_init(ptx::smem_addr(&ctrl->never), 1);
+        ctrl->wait.abort = 0;
+        ctrl->wait.limit_ns = p.wait_limit_ns;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmap_a);
+        ptx::prefetch_tmap(&tmap_b);
+        if (p.b3d) ptx::prefetch_tmap(&tmap_b2);
+    }
+    if (p.tma_store && warp == 2 && lane == 0) ptx::prefetch_tmap(&tmap_c);
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_addr(&ctrl->tmem_base), P128_TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = ctrl->tmem_base;
+    WaitCtl *wc = &ctrl->wait;
+    const uint32_t smem_base = ptx::smem_addr(smem);
+
+    if (warp == 0) {
+        if (lane == 0) p128_producer<kKind>(&tmap_a, &tmap_b, &tmap_b2, p, smem_base, ctrl, rank, wc);
+    } else if (warp == 1) {
+        if (rank == 0 && lane == 0) p128_mma<kKind>(p, smem_base, ctrl, tmem_base, wc);
+    } else {
+        p128_epilogue<kKind>(p, &tmap_c, ctrl, tmem_base, smem_base + STAGES * STAGE_BYTES, rank, warp, lane,
+                             wc);
+    }
+
+    __syncwarp();
+    ptx::tc_fence_before();
+    ptx::cluster_sync();  // no CTA leaves while the other may still signal or write it
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, P128_TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -1998,6 +2220,41 @@ bool launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap
     return true;
 }
 
+template <int kKind>
+int cluster_capacity(int size);
+
+// The small-M pair kernel: one 128 x p.bn tile per pair, so at most one wave
+// of co-resident pairs (false, nothing launched, beyond that).
+template <int kKind>
+bool launch_pair128(const CUtensorMap &ma64, const CUtensorMap &mb, const CUtensorMap &mb2, const CUtensorMap &mc,
+                    const Params &p, cudaStream_t stream)
+{
+    const int64_t tiles = p.tiles_m * p.tiles_n;
+    if (tiles < 1 || tiles > cluster_capacity<kKind>(2)) return false;
+    if (cudaFuncSetAttribute(umma_pair128_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * tiles));
+    cfg.blockDim = dim3(cta_threads<true>());
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, umma_pair128_kernel<kKind>, ma64, mb, mb2, mc, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
 // One-shot test hook (dgemm_test_inject_stall): applies to the next
 // tensor-core launch made by this host thread.
 thread_local uint64_t t_inject_limit_ns = 0;
@@ -2090,8 +2347,9 @@ int cluster_capacity(int size)
 // (4 is unused: it once named a two-pair cluster variant, since removed.)
 // 6 and 7: the pair kernels with the finer ring (32-deep K stages of the
 // K-major 16-bit kinds, see PairShape).
+// 8: the CTA pair for small M (128 x bn tiles, 64 rows of A per CTA).
 enum { kVariantAuto = 0, kVariantPair = 1, kVariantSingle = 2, kVariantSplit = 3, kVariantWide = 5,
-       kVariantPairFine = 6, kVariantWideFine = 7 };
+       kVariantPairFine = 6, kVariantWideFine = 7, kVariantPair128 = 8 };
 struct UmmaConfig {
     int variant;
     int bn;
@@ -2202,6 +2460,17 @@ UmmaConfig choose_config(const Params &p, int sm_count, bool pair_ok)
             }
         }
     }
+    // The small-M pair, by rule rather than by the model (its per-CTA stream
+    // rate is lower than the single-CTA kernel's: both CTAs' loads, and a
+    // round trip between them, gate every stage): 16-bit kinds, one band of
+    // rows and 48 to 76 tiles of 128 x 256, where it measured faster than
+    // every configuration above (FP16 127 x 12288 x 4096: TN 26.6 against
+    // 26.9 us, NN 26.8 against 28.6 us; TF32 and fewer tiles were slower).
+    if constexpr (!T::kTf32) {
+        const int64_t tiles = (p.N + BN - 1) / BN;
+        if (p.tiles_m == 1 && tiles >= 48 && tiles * 2 <= sm_count && tiles <= cluster_capacity<kKind>(2))
+            return {kVariantPair128, BN, 1};
+    }
     return best;
 }
 
@@ -2239,7 +2508,7 @@ bool launch_splitk(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorM
 template <int kKind>
 const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = false)
 {
-    static std::string names[10 + 9 * 9];  // [2 + 9 * 9] unused
+    static std::string names[10 + 9 * 9 + 9];  // [2 + 9 * 9] and [10 + 9 * 9] unused
     static std::once_flag once;
     std::call_once(once, [] {
         using T = Traits<kKind>;
@@ -2262,8 +2531,10 @@ const char *variant_name(int variant, int bn = BN, int split = 1, bool sk = fals
             names[2 + w * 9 + 1] = base + "_" + tile + "_tma";
             for (int S = 2; S <= 8; ++S)
                 names[2 + w * 9 + S] = base + "_splitk" + std::to_string(S) + "_" + tile + "_tma";
+            names[10 + 9 * 9 + w] = base + "_pair_" + tile + "_tma";
         }
     });
+    if (variant == kVariantPair128) return names[10 + 9 * 9 + bn / 32].c_str();
     if (variant == kVariantPair) return names[sk ? 4 + 9 * 9 : 0].c_str();
     if (variant == kVariantWide) return names[sk ? 5 + 9 * 9 : 3 + 9 * 9].c_str();
     if (variant == kVariantPairFine) return names[sk ? 7 + 9 * 9 : 6 + 9 * 9].c_str();
@@ -2296,11 +2567,11 @@ void set_ring(Params &p, bool split)
 
 // TMA-capable operands.  ma: A with 128-row boxes; mb_pair: B boxes of the
 // pair kernel (null if B cannot be described); make_b(bn, map) builds B's map
-// for 128 x bn tiles.
-template <int kKind, typename MakeB>
+// for 128 x bn tiles; make_a64(map) A's map with 64-row boxes.
+template <int kKind, typename MakeB, typename MakeA64>
 const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensorMap *mb_pair,
                          const CUtensorMap *mb_pair2, const CUtensorMap *ma_fine, const CUtensorMap *mb_fine,
-                         int pair3d, int64_t pair3d_cols, MakeB make_b, const CUtensorMap &mc,
+                         int pair3d, int64_t pair3d_cols, MakeB make_b, MakeA64 make_a64, const CUtensorMap &mc,
                          cudaStream_t stream, const DeviceInfo &dev)
 {
     UmmaConfig cfg = t_tune;
@@ -2317,6 +2588,28 @@ const char *dispatch_tma(const Params &p0, const CUtensorMap &ma, const CUtensor
                              : UmmaConfig{kVariantSingle, cfg.bn, 1};
     if (cfg.variant == kVariantAuto)
         cfg = choose_config<kKind>(p0, dev.sm_count, mb_pair != nullptr);
+    if (cfg.variant == kVariantPair128) {
+        // the small-M pair: B in boxes of bn / 2 rows (columns, N-major)
+        Params q = p0;
+        q.bn = cfg.bn;
+        q.tiles_m = (p0.M + BM - 1) / BM;
+        q.tiles_n = (p0.N + cfg.bn - 1) / cfg.bn;
+        q.stage_bytes = 2 * static_cast<int>(p128_half_bytes(cfg.bn));
+        q.stages = std::min(MAX_STAGES, STAGES * STAGE_BYTES / q.stage_bytes);
+        if ((cfg.bn / 2) % box_cols<kKind>() != 0) q.tma_store = 0;
+        CUtensorMap a64{}, bh{};
+        int b3d = 0;
+        const bool fits = !Traits<kKind>::kBNMajor || (cfg.bn / 2) % Traits<kKind>::kNBox == 0;
+        if (fits && make_a64(&a64) && make_b(cfg.bn / 2, &bh, &b3d)) {
+            q.b3d = b3d;
+            q.b3d_cols = b3d ? INT64_MAX : 0;
+            if (launch_pair128<kKind>(a64, bh, bh, mc, q, stream)) return variant_name<kKind>(kVariantPair128, cfg.bn);
+        }
+        // (a tile count beyond one wave of pairs, or a B the boxes cannot
+        // describe): the automatic choice among the other kernels
+        cfg = choose_config<kKind>(p0, dev.sm_count, mb_pair != nullptr);
+        if (cfg.variant == kVariantPair128) cfg = UmmaConfig{kVariantSingle, BN, 1};
+    }
     Params p = p0;
     if constexpr (!Traits<kKind>::kBNMajor) {
         if (cfg.variant == kVariantPairFine || cfg.variant == kVariantWideFine) {
@@ -2469,9 +2762,12 @@ const char *launch_kind(int64_t M, int64_t N, int64_t K, float alpha, const void
                 if (t_tune.variant == kVariantPairFine || t_tune.variant == kVariantWideFine)
                     ok_fine = make_map(&maf, dt, A, K, M, lda * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) &&
                               make_map(&mbf, dt, B, K, N, ldb * es, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+            auto make_a64 = [&](CUtensorMap *m) {
+                return make_map(m, dt, A, K, M, lda * es, T::BK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+            };
             return dispatch_tma<kKind>(p, ma, ok_pair ? &mbp : nullptr, ok_pair ? &mbp2 : nullptr,
                                        ok_fine ? &maf : nullptr, ok_fine ? &mbf : nullptr, pair3d, pair3d_cols,
-                                       make_b, mc, stream, dev);
+                                       make_b, make_a64, mc, stream, dev);
         }
     }
     t_tune = UmmaConfig{kVariantAuto, BN, 1};
@@ -2503,14 +2799,15 @@ const char *launch_umma(int kind, int64_t M, int64_t N, int64_t K, float alpha, 
 
 int umma_tune_next(int variant, int bn, int split)
 {
-    if (variant < kVariantAuto || variant > kVariantWideFine || variant == 4) return DGEMM_ERR_INVALID_ARG;
+    if (variant < kVariantAuto || variant > kVariantPair128 || variant == 4) return DGEMM_ERR_INVALID_ARG;
+    if (variant == kVariantPair128 && (bn < 128 || bn > BN || bn % 64 != 0)) return DGEMM_ERR_INVALID_ARG;
     if ((variant == kVariantSingle || variant == kVariantSplit) && (bn < 32 || bn > BN || bn % 32 != 0))
         return DGEMM_ERR_INVALID_ARG;
     if (variant == kVariantSplit && (split < 2 || split > 8)) return DGEMM_ERR_INVALID_ARG;
     const bool paired = variant == kVariantPair || variant == kVariantWide || variant == kVariantPairFine ||
                         variant == kVariantWideFine;
     if (paired && (split < kSkAuto || split > kSkOn)) return DGEMM_ERR_INVALID_ARG;
-    const bool sized = variant == kVariantSingle || variant == kVariantSplit;
+    const bool sized = variant == kVariantSingle || variant == kVariantSplit || variant == kVariantPair128;
     t_tune = UmmaConfig{variant, sized ? bn : BN, variant == kVariantSplit || paired ? split : 1};
     return DGEMM_OK;
 }

@@ -49,14 +49,16 @@ def configs(step: int, sms: int, M: int, N: int):
         return [(dg.TUNE_AUTO, 256, 1)]
     """Every (variant, bn, split) worth timing: the pair kernels (256 x 256
     and 256 x 512 tiles, each round-robin and with the stream-K tail, with
-    the ordinary and the finer stage ring), and for each tile width bn the single-CTA kernel
+    the ordinary and the finer stage ring; 128 x bn tiles of the small-M
+    pair), and for each tile width bn the single-CTA kernel
     and the splits that fit one wave (step 0: the FP32 SIMT call, automatic
     only)."""
     out = [(dg.TUNE_AUTO, 256, 1), (dg.TUNE_PAIR, 256, dg.SK_OFF), (dg.TUNE_PAIR, 256, dg.SK_ON),
            (dg.TUNE_PAIR_WIDE, 256, dg.SK_OFF),
            (dg.TUNE_PAIR_WIDE, 256, dg.SK_ON),
            (dg.TUNE_PAIR_FINE, 256, dg.SK_OFF), (dg.TUNE_PAIR_FINE, 256, dg.SK_ON),
-           (dg.TUNE_PAIR_WIDE_FINE, 256, dg.SK_OFF), (dg.TUNE_PAIR_WIDE_FINE, 256, dg.SK_ON)]
+           (dg.TUNE_PAIR_WIDE_FINE, 256, dg.SK_OFF), (dg.TUNE_PAIR_WIDE_FINE, 256, dg.SK_ON),
+           (dg.TUNE_PAIR128, 256, 1), (dg.TUNE_PAIR128, 192, 1), (dg.TUNE_PAIR128, 128, 1)]
     tiles_m = (M + 127) // 128
     for bn in range(256, 31, -step):
         out.append((dg.TUNE_SINGLE, bn, 1))

@@ -373,9 +373,15 @@ int dgemm_test_choose_config(int kind, int64_t M, int64_t N, int64_t K, int sm_c
  *           6, 7: as 1 and 5 with the finer stage ring of the K-major
  *              16-bit calls (gemm_f16_tn, gemm_bf16_tn): 32-deep K stages
  *              under the 64-byte swizzle, twice as many in the same
- *              shared memory; other calls take 1 or 5 instead.
+ *              shared memory; other calls take 1 or 5 instead;
+ *           8: CTA pair for small M, 128 x bn output tiles: one
+ *              tcgen05.mma of M = 128 over the pair, each CTA loading 64
+ *              rows of A and bn / 2 rows (columns, N-major) of B; one tile
+ *              per pair, so only problems of at most one wave of pairs
+ *              (the call chooses as usual otherwise).
  *   bn:    tile width for variants 2 and 3: 32..256 in steps of 32; the
- *          NN 16-bit calls need a multiple of 64.  Ignored otherwise.
+ *          NN 16-bit calls need a multiple of 64.  For variant 8: 128, 192
+ *          or 256 (the NN 16-bit calls: 128 or 256).  Ignored otherwise.
  *   split: 2..8 for variant 3 (lowered to the number of K blocks when K is
  *          shorter, so that every CTA has work); for variants 1, 5, 6 and 7
  *          the stream-K mode: 0 automatic, 1 whole tiles only, 2 cut the first

@@ -126,8 +126,11 @@ def test_last_kernel_empty_before_any_launch(L):
 def test_tune_next_validates_on_host(L):
     # out-of-range requests are refused and record nothing (no device needed)
     assert L.dgemm_tune_next(-1, 256, 1) == 1
-    assert L.dgemm_tune_next(8, 256, 1) == 1
+    assert L.dgemm_tune_next(9, 256, 1) == 1
     assert L.dgemm_tune_next(4, 256, 1) == 1     # 4 names no variant
+    assert L.dgemm_tune_next(8, 192, 1) == 0     # the small-M pair: bn 128, 192 or 256
+    assert L.dgemm_tune_next(8, 96, 1) == 1
+    assert L.dgemm_tune_next(8, 160, 1) == 1
     assert L.dgemm_tune_next(6, 256, 2) == 0     # the finer-ring pair variants
     assert L.dgemm_tune_next(7, 256, 3) == 1     # (their split is a stream-K mode: 0..2)
     assert L.dgemm_tune_next(0, 0, 0) == 0

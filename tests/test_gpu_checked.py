@@ -90,6 +90,8 @@ FAMILIES = [
     ("f16_tn", (2304, 2304, 512), (0, 0, 0), (1, 256, 2), "_sk_"),        # pair, stream-K tail
     ("bf16_nn", (300, 704, 200), (0, 0, 0), (2, 128, 1), "_128x128"),     # single-CTA kernel
     ("f16_tn", (100, 1000, 2048), (0, 0, 0), None, "_splitk"),            # split-K in clusters (DSMEM)
+    ("f16_tn", (100, 1000, 520), (0, 0, 0), (8, 192, 1), "_pair_128x192"),  # small-M pair, ragged N
+    ("tf32", (40, 2048, 264), (0, 0, 0), (8, 256, 1), "_pair_128x256"),     # small-M pair, N-major B
     ("tf32", (300, 520, 130), (1, 2, 0), None, "_cpasync"),               # cp.async producer
     ("f16_nn", (300, 520, 130), (1, 2, 0), None, "_ldst"),                # register-path producer
     ("f16_tn", (257, 300, 72), (0, 0, 3), None, "umma_f16_tn"),           # unaligned C: row-by-row stores
