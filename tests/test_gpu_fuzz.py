@@ -62,3 +62,39 @@ def test_fuzz_case_matches_oracle(case):
     assert dg.device_status(clear=False) == dg.OK
     assert torch.isfinite(got).all(), dg.last_kernel()
     assert parity.worst_ratio(path, got, A, B, C, alpha, beta) <= 1.0, dg.last_kernel()
+
+
+# The small-M pair (tuning variant 8) on seeded random problems: one or two
+# bands of rows, any N (most within one wave of pairs), pitch padding, base
+# offsets and both betas.  Where the operands rule the kernel out (pitches
+# TMA cannot describe, too many tiles) the call chooses another one; every
+# result is compared in full with the oracle.
+def _pair128_cases(n=48, seed=20261203):
+    rng = np.random.default_rng(seed)
+    paths = [p for p in parity.PATHS if p != "f32"]
+    out = []
+    for i in range(n):
+        path = paths[i % len(paths)]
+        M = int(rng.integers(1, 257))
+        # N and K multiples of 8 and pads / offsets of 8 or 16 elements keep
+        # the pitches and bases TMA-describable, so that this kernel runs;
+        # one case in eight pads by 3 (another kernel must take it)
+        N = 8 * math.ceil(math.exp(rng.uniform(math.log(64), math.log(6000))) / 8)
+        K = 8 * math.ceil(math.exp(rng.uniform(math.log(16), math.log(1500))) / 8)
+        pad = tuple(int(x) for x in rng.choice([0, 0, 0, 8, 16], size=3))
+        if i % 8 == 7:
+            pad = (3, 0, 0)
+        offset = tuple(int(x) for x in rng.choice([0, 0, 0, 8], size=3))
+        alpha = float(rng.choice([1.0, -0.5, 0.75]))
+        beta = float(rng.choice([0.0, 1.0, -0.75]))
+        bn = int(rng.choice([128, 192, 256]))
+        out.append((path, (M, N, K), pad, offset, alpha, beta, (8, bn, 1)))
+    return out
+
+
+PAIR128_CASES = _pair128_cases()
+
+
+@pytest.mark.parametrize("case", PAIR128_CASES, ids=[_id(c) for c in PAIR128_CASES])
+def test_fuzz_pair128_matches_oracle(case):
+    test_fuzz_case_matches_oracle(case)
