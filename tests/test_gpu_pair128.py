@@ -105,3 +105,20 @@ def test_pair128_stall_times_out_cleanly():
     got, _, _ = parity.run("f16_tn", A, B, C, 1.0, 0.0)
     assert dg.device_status(clear=True) == dg.OK
     assert parity.worst_ratio("f16_tn", got, A, B, C, 1.0, 0.0) <= 1.0
+
+
+@pytest.mark.parametrize("path", ["f16_tn", "f16_nn", "bf16_tn", "bf16_nn", "tf32"])
+def test_automatic_choice_for_the_skinny_workload(path):
+    """One band of rows and 48 tiles of 128 x 256: the 16-bit kinds take the
+    small-M pair (measured fastest there), TF32 does not (it measured slower)."""
+    import ctypes
+    import dense_gemm_09_gb300 as dg
+    kind = {"f16_tn": 0, "tf32": 1, "bf16_tn": 2, "f16_nn": 3, "bf16_nn": 4}[path]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out = [ctypes.c_int() for _ in range(3)]
+    assert dg.lib().dgemm_test_choose_config(kind, 127, 12288, 4096, sms, *(ctypes.byref(o) for o in out)) == dg.OK
+    v, bn, sp = (o.value for o in out)
+    if path == "tf32":
+        assert v != dg.TUNE_PAIR128, (v, bn, sp)
+    else:
+        assert (v, bn) == (dg.TUNE_PAIR128, 256), (v, bn, sp)
