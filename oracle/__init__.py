@@ -17,7 +17,7 @@ Sources (page title, section):
     C all row-major; TN: B stored N x K.
   * "SGEMM CUDA代码学习", "第 5 步" -- BF16 among the tensor-core precisions.
 
-Acceptance, per element (the tolerance rule the method is judged by):
+Acceptance, per element (the tolerance rule results are checked against):
     |C_gpu - ref| <= tol * (|A||B|)_ij + tol * |beta * c_ij|
 """
 from __future__ import annotations
