@@ -178,6 +178,8 @@ def _config(paths_run, shape, world):
             "parallelism": "replicas x%d" % world}
 
 
+# the headline metric; both arms print it
+METRIC = "GEMM TFLOPS (2MNK/s) per dtype at M=N=8192,K=4096; % of dense peak"
 L2_NOTE = "flushed before every GEMM (512 MiB write + 256 MiB read, outside the timed events)"
 
 
@@ -393,7 +395,7 @@ def run_ours(args):
     clocks = clk.summary()
     default_run = tuple(paths_run) == PATHS and (Mx, Nx, Kx) == (M, N, K)
     line = {
-        "metric": "GEMM TFLOPS (2MNK/s) per dtype at M=N=8192,K=4096; % of dense peak",
+        "metric": METRIC,
         "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32+tf32+f16(f32 acc)" if default_run
@@ -530,7 +532,7 @@ def run_reference(args):
     value = statistics.mean(rates)
     line = {
         "impl": "reference",
-        "metric": "GEMM TFLOPS (2MNK/s) per dtype at M=N=8192,K=4096; % of dense peak",
+        "metric": METRIC,
         "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / max(args.steps, 1), 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
